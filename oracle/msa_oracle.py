@@ -274,7 +274,7 @@ def chunk_forward(q, k, v, lay, kv_doc_starts, sel, hi, d, c, G, scale):
     kc = _gather(k, k0 + kp, hi)                                               # [nk, D]
     vc = _gather(v, k0 + kp, hi)
     mask = kp[None, :] <= qp[:, None]                                          # [nq, nk]
-    s = scale * np.einsum("gqd,kd->gqk", qc, kc)
+    s = scale * (qc @ kc.T)                                                   # [G, nq, nk]
     s = np.where(mask[None], s, -np.inf)
     mx = np.max(s, axis=2, keepdims=True)
     mx = np.where(np.isfinite(mx), mx, 0.0)
@@ -282,7 +282,7 @@ def chunk_forward(q, k, v, lay, kv_doc_starts, sel, hi, d, c, G, scale):
     with np.errstate(divide="ignore"):
         lse = mx[..., 0] + np.log(e.sum(axis=2))
     p = np.where(mask[None], np.exp(s - lse[..., None]), 0.0)
-    return qp, np.einsum("gqk,kd->gqd", p, vc), lse
+    return qp, p @ vc, lse
 
 
 def chunk_backward(q, k, v, do, oc, lc, lay, kv_doc_starts, sel, hi, d, c, G, scale):
@@ -307,14 +307,15 @@ def chunk_backward(q, k, v, do, oc, lc, lay, kv_doc_starts, sel, hi, d, c, G, sc
     kc = _gather(k, k0 + kp, hi)
     vc = _gather(v, k0 + kp, hi)
     mask = (kp[None, :] <= qp[:, None])[None]
-    s = scale * np.einsum("gqd,kd->gqk", qc, kc)
+    s = scale * (qc @ kc.T)                                                   # [G, nq, nk]
     p = np.where(mask, np.exp(s - lc[..., None]), 0.0)
-    dp = np.einsum("gqd,kd->gqk", doc_, vc)
+    dp = doc_ @ vc.T
     delta = np.sum(doc_ * oc, axis=2)
     ds = p * (dp - delta[..., None])
-    dq = scale * np.einsum("gqk,kd->gqd", ds, kc)
-    dk = scale * np.einsum("gqk,gqd->kd", ds, qc)
-    dv = np.einsum("gqk,gqd->kd", p, doc_)
+    dq = scale * (ds @ kc)
+    n = G * qp.size                                                           # sum over (head, query)
+    dk = scale * (ds.reshape(n, -1).T @ qc.reshape(n, D))
+    dv = p.reshape(n, -1).T @ doc_.reshape(n, D)
     return qp, dq, kp, dk, dv
 
 
