@@ -1,0 +1,366 @@
+#!/usr/bin/env python
+"""Benchmark of the MSA block-sparse attention backward on GB300.
+
+One step = the whole hot path over one batch: msa_build_k2q (CSR),
+msa_build_tasks (task rows + CTA walk), and msa_bwd (preprocess D, main
+KV-parallel tcgen05 kernel, postprocess casts).  Inputs (Q, K, V, dO drawn
+bf16 N(0,1); O and LSE produced by msa_fwd) are resident in HBM before the
+timed region; they are larger than L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long128k]
+    python bench.py --impl reference     # the fp64 CPU oracle on a bounded sample
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own
+independent batch (seed = rank): no data-path collective, weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MSA backward effective TFLOP/s (selected blocks) and % of GB300 bf16 peak"
+UNIT = "TFLOP/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["bf16_tflops"]), float(m["bf16_tflops_sustained"]), float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def _rank():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.gpu)], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(parts)
+            except Exception:
+                pass
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (bounded sample)
+# ---------------------------------------------------------------------------
+def oracle_sample(pb, host, budget_s: float, seed: int = 1):
+    """Time the fp64 oracle backward on random (index head, chunk) units of the
+    workload until about budget_s of CPU time; returns (TFLOP/s, seconds,
+    units, flop).  O/LSE of each unit come from the oracle forward (untimed)."""
+    from oracle import msa_oracle as O
+    lay = O.DocLayout(pb.cu_seqlens, pb.block, pb.chunk)
+    rng = np.random.default_rng(seed)
+    q, k, v, do = host
+    G = pb.group
+    t_spent, flop, units = 0.0, 0, 0
+    while t_spent < budget_s and units < 100000:
+        g = int(rng.integers(0, lay.NC))
+        hi = int(rng.integers(0, pb.num_index_heads))
+        d = int(np.searchsorted(lay.chunk_off, g, side="right") - 1)
+        c = g - int(lay.chunk_off[d])
+        _, oc, lc = O.chunk_forward(q, k, v, lay, pb.kv_doc_starts, pb.sel, hi, d, c, G, pb.softmax_scale)
+        oc = O.bf16_to_f64(O.f64_to_bf16(oc))
+        lc = lc.astype(np.float32).astype(np.float64)
+        t0 = time.perf_counter()
+        O.chunk_backward(q, k, v, do, oc, lc, lay, pb.kv_doc_starts, pb.sel, hi, d, c, G, pb.softmax_scale)
+        t_spent += time.perf_counter() - t0
+        nq = lay.chunk_positions(d, c).size
+        flop += nq * G * int((pb.sel[hi, g] >= 0).sum()) * 10 * pb.block * pb.head_dim
+        units += 1
+    return flop / t_spent / 1e12, t_spent, units, flop
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank, world, _ = _rank()
+    if rank != 0:
+        return 0
+    from block_sparse_top_attn_gb300 import workloads as W
+    pb = W.make_problem(args.workload, values=False)
+    host = _host_values(pb)
+    for _ in range(args.warmup):
+        oracle_sample(pb, host, 0.5, seed=99)
+    times, flops = [], 0
+    tot_t = 0.0
+    for s in range(args.steps):
+        v, t, units, f = oracle_sample(pb, host, args.ref_budget, seed=s)
+        tot_t += t
+        flops += f
+    value = flops / tot_t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "tokens": pb.total_tokens, "q_heads": pb.num_q_heads,
+                       "index_heads": pb.num_index_heads, "topk": pb.topk},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+                             "sample": f"{args.steps} steps x ~{args.ref_budget:.0f} s of random (index head, "
+                                       f"query chunk) units of the workload, fp64 NumPy backward"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _host_values(pb):
+    """Host bf16 bit arrays for the oracle leg: drawn on the GPU when one is
+    present (fast), else with numpy."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            from block_sparse_top_attn_gb300 import workloads as W
+            vals = W.device_values(pb, "cuda", seed=0)
+            return tuple(t.view(torch.int16).cpu().numpy().view(np.uint16) for t in vals)
+    except Exception:
+        pass
+    rng = np.random.default_rng(12345)
+    from block_sparse_top_attn_gb300 import workloads as W
+    T, Hq, D, Hkv, Wr = pb.total_tokens, pb.num_q_heads, pb.head_dim, pb.num_index_heads, pb.kv_rows
+    return (W._normal_bf16(rng, (T, Hq, D)), W._normal_bf16(rng, (Wr, Hkv, D)), W._normal_bf16(rng, (Wr, Hkv, D)),
+            W._normal_bf16(rng, (T, Hq, D)))
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+def _traffic_record():
+    """Per-launch DRAM bytes of the main kernel from the committed ncu summary,
+    valid only while the kernel source it was taken on is unchanged."""
+    src = os.path.join(ROOT, "block_sparse_top_attn_gb300", "csrc", "msa_bwd.cu")
+    sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    path = os.path.join(ROOT, "profiles", "bwd_main_long128k.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"source_sha1:\s*([0-9a-f]{40})", txt)
+    t = re.search(r"traffic_bytes_per_launch_full:\s*([0-9.eE+]+)", txt)
+    if m and t and m.group(1) == sha:
+        return float(t.group(1))
+    return None
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    rank, world, local = _rank()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from block_sparse_top_attn_gb300 import binding as B
+    from block_sparse_top_attn_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    pb = W.make_problem(args.workload, values=False, seed=rank)
+    prob = B.make_problem(pb.cu_seqlens, pb.kv_doc_starts, pb.kv_rows, pb.num_q_heads, pb.topk, pb.softmax_scale,
+                          device=dev)
+    sel = torch.from_numpy(pb.sel).to(dev)
+    q, k, v, do = W.device_values(pb, dev, seed=rank)
+    o, lse, st = B.forward(prob, sel, q, k, v)
+    torch.cuda.synchronize()
+    if int(st[0].item()) != 0:
+        raise B.MSAError(int(st[0].item()), "msa_fwd")
+    flop = W.effective_flops(pb)
+    bw = B.Backward(prob, task_tile_chunks=args.tile)
+    stream = torch.cuda.current_stream()
+    nsteps_events = []
+
+    def step(ev=None):
+        bw.build_tables(sel)
+        bw.backward_stage(B.MSA_STAGE_PREPROCESS, q, k, v, o, do, lse)
+        if ev is not None:
+            ev[0].record(stream)
+        bw.backward_stage(B.MSA_STAGE_MAIN, q, k, v, o, do, lse)
+        if ev is not None:
+            ev[1].record(stream)
+        bw.backward_stage(B.MSA_STAGE_POSTPROCESS, q, k, v, o, do, lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    bw.check_status()
+    n_tasks = bw.num_tasks()
+
+    main_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(main_ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    bw.check_status()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    main_ms = sum(a.elapsed_time(b) for a, b in main_ev) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = world * flop / (ms * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers (pinned), copies timed
+    pin = lambda t: t.cpu().pin_memory()
+    host_in = {"q": pin(q), "k": pin(k), "v": pin(v), "o": pin(o), "do": pin(do), "lse": pin(lse), "sel": pin(sel)}
+    host_out = {"dq": torch.empty_like(bw.dq, device="cpu").pin_memory(),
+                "dk": torch.empty_like(bw.dk, device="cpu").pin_memory(),
+                "dv": torch.empty_like(bw.dv, device="cpu").pin_memory()}
+    dev_in = {"q": q, "k": k, "v": v, "o": o, "do": do, "lse": lse, "sel": sel}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for name, t in host_in.items():
+            dev_in[name].copy_(t, non_blocking=True)
+        bw.run(sel, q, k, v, o, do, lse)
+        host_out["dq"].copy_(bw.dq, non_blocking=True)
+        host_out["dk"].copy_(bw.dk, non_blocking=True)
+        host_out["dv"].copy_(bw.dv, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    bw.check_status()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = world * flop / (e2e_ms * 1e-3) / 1e12
+
+    burst, sustained, hbm, src = _peaks()
+    achieved = flop / (main_ms * 1e-3) / 1e12
+    traffic = _traffic_record()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "tokens": pb.total_tokens, "documents": pb.num_docs,
+                   "q_heads": pb.num_q_heads, "index_heads": pb.num_index_heads, "head_dim": pb.head_dim,
+                   "block": pb.block, "chunk": pb.chunk, "topk": pb.topk, "tasks": n_tasks,
+                   "effective_tflop_per_step": flop / 1e12, "task_tile_chunks": args.tile,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "fraction_of_peak": {"value": value / sustained, "peak_tflops": sustained,
+                             "peak_kind": f"bf16 sustained ({src})"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
+                     "frac": achieved / sustained, "traffic": traffic, "kernel": "bwd_main",
+                     "kernel_ms": main_ms, "peak_kind": f"bf16 sustained, of {src}"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * 14,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = tuple(t.view(torch.int16).numpy().view(np.uint16) for t in (host_in["q"], host_in["k"],
+                                                                             host_in["v"], host_in["do"]))
+        cv, ct, units, cf = oracle_sample(pb, host, args.cpu_budget)
+        line["cpu_baseline"] = {"value": cv, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+                                "sample": f"{units} random (index head, query chunk) units, {cf / 1e9:.1f} GFLOP, "
+                                          f"{ct:.1f} s fp64 NumPy backward"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long128k")
+    ap.add_argument("--tile", type=int, default=512, help="query chunks per task tile (0 = untiled)")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-budget", type=float, default=8.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,45 @@
+// Host-side helpers shared by the translation units of the MSA library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/msa.h"
+
+namespace msa {
+
+constexpr int kHeadDim = 128;
+constexpr int kBlock = 64;
+constexpr int kChunk = 8;
+constexpr int kGroup = 16;
+constexpr int kMaxTopk = 32;
+// Largest number of key-block rows one document set may have: the CSR
+// scatter keeps one cursor per row of a group's documents in shared memory.
+constexpr int kMaxRows = 49152;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Host-checkable problem validity (shapes the kernels are built for).
+int check_problem(const msa_problem* p);
+
+// Scatter-group size (query chunks per group) of the CSR build.
+inline int64_t k2q_group_chunks(int64_t nc) {
+  int64_t g = (nc + 127) / 128;
+  return g < 64 ? 64 : g;
+}
+inline int64_t num_tiles(int64_t nc, int32_t tile_chunks) {
+  return tile_chunks > 0 ? (nc + tile_chunks - 1) / tile_chunks : 1;
+}
+
+size_t k2q_ws_bytes(const msa_problem* p);
+size_t tasks_ws_bytes(const msa_problem* p, int32_t tile_chunks);
+size_t bwd_ws_bytes(const msa_problem* p);
+
+int sm_count_current(int32_t* out);
+int check_device_current();
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
+
+}  // namespace msa

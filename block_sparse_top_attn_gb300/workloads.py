@@ -220,3 +220,34 @@ def make_problem(name: str | None = None, *, seed: int = 0, lengths=None,
         q = k = v = do = None
     return Problem(name or "custom", cu, kv_starts, kv_rows, hq, num_index_heads, head_dim,
                    block, chunk, topk, sel, q, k, v, do, float(head_dim) ** -0.5)
+
+
+def device_values(pb: Problem, device="cuda", seed: int = 0):
+    """bf16 N(0, 1) Q, K, V, dO drawn on the device with torch's seeded Philox
+    generator (for workloads whose host draw would take tens of seconds).
+    Returns torch bf16 tensors (q, k, v, do); the host draw order is kept."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    T, Hq, Hkv, D, W = pb.total_tokens, pb.num_q_heads, pb.num_index_heads, pb.head_dim, pb.kv_rows
+
+    def draw(shape):
+        out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        flat = out.view(-1)
+        step = 1 << 28
+        for s in range(0, flat.numel(), step):
+            n = min(step, flat.numel() - s)
+            flat[s:s + n] = torch.randn(n, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+        return out
+
+    return draw((T, Hq, D)), draw((W, Hkv, D)), draw((W, Hkv, D)), draw((T, Hq, D))
+
+
+def effective_flops(pb: Problem) -> int:
+    """Effective FLOP of the backward over full selected blocks: every
+    (query, q-head, selected block) costs 5 GEMMs x 2 x block x head_dim."""
+    lengths = np.diff(pb.cu_seqlens.astype(np.int64))
+    chunk_len = np.concatenate([np.minimum(pb.chunk, n - np.arange(0, n, pb.chunk)) for n in lengths])
+    slots = (pb.sel >= 0).sum(axis=2)                      # [Hi, NC]
+    rows = int((slots * chunk_len[None, :]).sum()) * pb.group
+    return rows * 10 * pb.block * pb.head_dim
