@@ -375,6 +375,8 @@ __global__ void __launch_bounds__(128, 1)
 
 }  // namespace msa
 
+#include "msa_bwd_ws.cuh"
+
 using namespace msa;
 
 extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -406,12 +408,14 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
   w += round_up(sizeof(float) * W * Hkv * kHeadDim, 256);
   const int64_t zero_n4 = (reinterpret_cast<float*>(w) - dq_acc) / 4;
 
+  // loads: Q/dO boxes of 8 tokens x 16 heads x 64 dims, K/V boxes of 64 keys x 64 dims;
+  // reduce-adds: dQ boxes of 2 tokens x 16 heads x 32 dims, dK/dV of 32 keys x 32 dims (fp32)
   CUtensorMap tmQ, tmdO, tmK, tmV, tmdQ, tmdK, tmdV;
   bool ok = make_tmap_3d(&tmQ, q, false, T, Hq, 64, 16, 8) && make_tmap_3d(&tmdO, dout, false, T, Hq, 64, 16, 8) &&
             make_tmap_3d(&tmK, k, false, W, Hkv, 64, 1, 64) && make_tmap_3d(&tmV, v, false, W, Hkv, 64, 1, 64) &&
-            make_tmap_3d(&tmdQ, dq_acc, true, T, Hq, 32, 16, 8) &&
-            make_tmap_3d(&tmdK, dk_acc, true, W, Hkv, 32, 1, 64) &&
-            make_tmap_3d(&tmdV, dv_acc, true, W, Hkv, 32, 1, 64);
+            make_tmap_3d(&tmdQ, dq_acc, true, T, Hq, 32, 16, 2) &&
+            make_tmap_3d(&tmdK, dk_acc, true, W, Hkv, 32, 1, 32) &&
+            make_tmap_3d(&tmdV, dv_acc, true, W, Hkv, 32, 1, 32);
   if (!ok) return MSA_ERR_CUDA;
 
   if (stages & ~(uint32_t)MSA_STAGE_ALL) return MSA_ERR_INVALID_ARGUMENT;
@@ -419,7 +423,7 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
     preprocess_kernel<<<sms * 8, 256, 0, st>>>(reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout),
                                              delta, T * Hq, reinterpret_cast<float4*>(dq_acc), zero_n4, d_status);
   if (stages & MSA_STAGE_MAIN) {
-  if (cudaFuncSetAttribute(bwd_main_v0, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)v0::SMEM) != cudaSuccess)
+  if (cudaFuncSetAttribute(bwd_main_ws, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ws::SMEM) != cudaSuccess)
     return MSA_ERR_CUDA;
   const int64_t bound = msa_grid_launch_bound(task_cap, sms);
   const int grid = (int)(bound < sms ? (bound < 1 ? 1 : bound) : sms);
@@ -427,7 +431,7 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
   a.lse = lse; a.delta = delta; a.meta = task_meta; a.q_rows = task_q_rows; a.q_pos = task_q_pos; a.walk = walk;
   a.kv_doc_starts = p->kv_doc_starts; a.Hq = (int)Hq; a.scale_log2 = p->softmax_scale * kLog2e;
   a.scale = p->softmax_scale; a.status = d_status;
-  bwd_main_v0<<<grid, 128, v0::SMEM, st>>>(tmQ, tmdO, tmK, tmV, tmdQ, tmdK, tmdV, a);
+  bwd_main_ws<<<grid, ws::kThreads, ws::SMEM, st>>>(tmQ, tmdO, tmK, tmV, tmdQ, tmdK, tmdV, a);
   }
   if (stages & MSA_STAGE_POSTPROCESS)
     postprocess_kernel<<<sms * 8, 256, 0, st>>>(

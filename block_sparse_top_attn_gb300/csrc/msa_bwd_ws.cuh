@@ -1,0 +1,446 @@
+// Warp-specialised, pipelined main backward kernel (sm_103a).
+//
+// Roles (14 warps, 448 threads, one CTA per SM, persistent over the walk):
+//   warp 0      TMA producer: K/V once per bucket segment (K double-buffered,
+//               V single), Q/dO per task into a 2-stage ring.
+//   warp 1      MMA issuer (one lane): S/dP of task j+1 before dV/dK/dQ of
+//               task j, so the tensor core works while task j's softmax runs.
+//   warps 2-9   softmax / dS: TMEM -> registers -> P, dS (bf16, swizzled smem).
+//               Warp w owns TMEM lanes 32*(w%4).. and key columns 32*((w-2)/4)..
+//   warps 10-13 reduce: dQ per task and dK/dV per segment, TMEM -> swizzled
+//               4 KB fp32 staging per warp -> TMA bulk reduce-add.
+//
+// TMEM (512 columns): S[2] at 0/128, dP[2] at 64/192, dQ at 256 (128 cols),
+// dK^T at 384, dV^T at 448 (64 cols each; lane = head-dim index).
+//
+// Every mbarrier wait is bounded (kWaitLimitNs) and also gives up when any
+// role has raised the shared abort flag; the status word records the timeout.
+#pragma once
+
+namespace msa {
+namespace ws {
+
+constexpr int kWarps = 14;
+constexpr int kThreads = kWarps * 32;
+constexpr int kLoadWarp = 0, kMmaWarp = 1, kComp0 = 2, kNumComp = 8, kRed0 = 10, kNumRed = 4;
+
+constexpr uint32_t OFF_QDO = 0;          // 2 stages x (Q 32 KB | dO 32 KB)
+constexpr uint32_t QDO_STAGE = 65536;
+constexpr uint32_t DO_IN_STAGE = 32768;
+constexpr uint32_t OFF_K = 131072;       // 2 stages x 16 KB
+constexpr uint32_t OFF_V = 163840;       // 16 KB
+constexpr uint32_t OFF_P = 180224;       // 16 KB, [128 rows][64 keys] bf16
+constexpr uint32_t OFF_DS = 196608;      // 16 KB
+constexpr uint32_t OFF_ST = 212992;      // 4 warps x 4 KB fp32 staging
+constexpr uint32_t OFF_BAR = 229376;
+constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+
+enum : int {
+  QDO_FULL = 0, QDO_EMPTY = 2, KV_FULL = 4, K_EMPTY = 6, V_EMPTY = 8, S_FULL = 9, S_EMPTY = 11,
+  PDS_FULL = 13, PDS_EMPTY = 14, DQ_FULL = 15, DQ_EMPTY = 16, DKV_FULL = 17, DKV_EMPTY = 18, DRAIN = 19,
+  NUM_BARS = 20
+};
+
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_DQ = 256, COL_DK = 384, COL_DV = 448;
+__device__ __forceinline__ uint32_t col_s(uint32_t st) { return st * 128; }
+__device__ __forceinline__ uint32_t col_dp(uint32_t st) { return st * 128 + 64; }
+
+// The CTA's task sequence: walk units blockIdx.x, +gridDim.x, ...; each unit a
+// run of R consecutive rows (full units) or a strided set of tail rows.
+struct Walk {
+  int n, R, full, grid;
+  int u, i, cnt, t0, step;
+  __device__ __forceinline__ void setup() {
+    if (u >= grid) return;
+    if (u < full) {
+      t0 = u * R; step = 1; cnt = R;
+    } else {
+      step = grid - full; t0 = full * R + (u - full); cnt = (n - t0 + step - 1) / step;
+    }
+  }
+  __device__ __forceinline__ void init(const int32_t* walk) {
+    n = walk[MSA_WALK_ROWS]; R = walk[MSA_WALK_ROWS_PER_CTA];
+    full = walk[MSA_WALK_FULL]; grid = walk[MSA_WALK_GRID];
+    u = blockIdx.x; i = 0;
+    setup();
+  }
+  __device__ __forceinline__ int take() {  // current task or -1, then advance
+    if (u >= grid) return -1;
+    const int t = t0 + i * step;
+    if (++i >= cnt) { u += gridDim.x; i = 0; setup(); }
+    return t;
+  }
+};
+
+// Current / next task of the sequence, with the bucket key of each.
+struct Seq {
+  Walk w;
+  int cur, nxt;
+  __device__ __forceinline__ void init(const int32_t* walk) {
+    w.init(walk);
+    cur = w.take();
+    nxt = w.take();
+  }
+  __device__ __forceinline__ void advance() {
+    cur = nxt;
+    nxt = w.take();
+  }
+};
+
+__device__ __forceinline__ int64_t bucket_key(const int32_t* meta, int t) {
+  return (static_cast<int64_t>(meta[(int64_t)t * MSA_TASK_META_COLS]) << 32) |
+         static_cast<uint32_t>(meta[(int64_t)t * MSA_TASK_META_COLS + 1]);
+}
+
+struct Shared {
+  uint64_t bar[NUM_BARS];
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Single-thread wait.  Gives up (false) on timeout, or as soon as another role
+// has aborted unless honor_abort is false (used for the final MMA drain).
+__device__ __forceinline__ bool wait_bar(Shared* sh, int idx, uint32_t parity, int32_t* status,
+                                         bool honor_abort = true) {
+  uint64_t* bar = &sh->bar[idx];
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (honor_abort && *reinterpret_cast<volatile int*>(&sh->abort)) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      set_status(status, MSA_ERR_TIMEOUT);
+      *reinterpret_cast<volatile int*>(&sh->abort) = 1;
+      return false;
+    }
+  }
+}
+
+// Warp-level wait: lane 0 polls, the outcome is broadcast so the warp stays
+// converged for the warp-collective tcgen05.ld that follows.
+__device__ __forceinline__ bool wait_bar_warp(Shared* sh, int idx, uint32_t parity, int32_t* status) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(sh, idx, parity, status) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+}  // namespace ws
+
+__global__ void __launch_bounds__(ws::kThreads, 1)
+    bwd_main_ws(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                const __grid_constant__ CUtensorMap tmdQ, const __grid_constant__ CUtensorMap tmdK,
+                const __grid_constant__ CUtensorMap tmdV, MainArgs a) {
+  using namespace ws;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Shared* sh = reinterpret_cast<Shared*>(sm + OFF_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    const uint32_t counts[NUM_BARS] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, kNumComp, kNumComp, kNumComp, 1,
+                                       1, kNumRed, 1, kNumRed, 1};
+    for (int i = 0; i < NUM_BARS; ++i) mbar_init(&sh->bar[i], counts[i]);
+    sh->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&sh->tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+  const int32_t* meta = a.meta;
+
+  if (!status_bad(a.status)) {
+    if (warp == kLoadWarp) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmdO);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        Seq s;
+        s.init(a.walk);
+        uint32_t nq = 0, nseg = 0;
+        int64_t prev = -1;
+        while (s.cur >= 0) {
+          const int t = s.cur;
+          const int64_t key = bucket_key(meta, t);
+          const int hi = meta[(int64_t)t * MSA_TASK_META_COLS];
+          if (key != prev) {
+            const int d = meta[(int64_t)t * MSA_TASK_META_COLS + 4];
+            const int b = meta[(int64_t)t * MSA_TASK_META_COLS + 5];
+            const uint32_t kst = nseg & 1;
+            if (!wait_bar(sh, K_EMPTY + kst, ((nseg >> 1) & 1) ^ 1, a.status)) break;
+            if (!wait_bar(sh, V_EMPTY, (nseg & 1) ^ 1, a.status)) break;
+            const int kvrow = a.kv_doc_starts[d] + b * 64;
+            uint64_t* fb = &sh->bar[KV_FULL + kst];
+            mbar_arrive_expect_tx(fb, 32768u);
+            tma_load_3d(sm + OFF_K + kst * 16384, &tmK, fb, 0, hi, kvrow);
+            tma_load_3d(sm + OFF_K + kst * 16384 + 8192, &tmK, fb, 64, hi, kvrow);
+            tma_load_3d(sm + OFF_V, &tmV, fb, 0, hi, kvrow);
+            tma_load_3d(sm + OFF_V + 8192, &tmV, fb, 64, hi, kvrow);
+            ++nseg;
+            prev = key;
+          }
+          const uint32_t qst = nq & 1;
+          if (!wait_bar(sh, QDO_EMPTY + qst, ((nq >> 1) & 1) ^ 1, a.status)) break;
+          const int tok0 = a.q_rows[(int64_t)t * 8];
+          uint64_t* fb = &sh->bar[QDO_FULL + qst];
+          uint8_t* st = sm + OFF_QDO + qst * QDO_STAGE;
+          mbar_arrive_expect_tx(fb, 65536u);
+          tma_load_3d(st, &tmQ, fb, 0, hi * 16, tok0);
+          tma_load_3d(st + 16384, &tmQ, fb, 64, hi * 16, tok0);
+          tma_load_3d(st + DO_IN_STAGE, &tmdO, fb, 0, hi * 16, tok0);
+          tma_load_3d(st + DO_IN_STAGE + 16384, &tmdO, fb, 64, hi * 16, tok0);
+          ++nq;
+          s.advance();
+        }
+      }
+    } else if (warp == kMmaWarp) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t ID_S = idesc_bf16_f32(128, 64, false, false);
+        constexpr uint32_t ID_T = idesc_bf16_f32(128, 64, true, true);
+        constexpr uint32_t ID_Q = idesc_bf16_f32(128, 128, false, true);
+        const uint32_t sb = smem_u32(sm);
+        Seq s;
+        s.init(a.walk);
+        uint32_t j = 0, nseg = 0;
+        int64_t prev = -1;
+        // pending B: task index j-1 and its segment facts
+        uint32_t pb_j = 0, pb_kst = 0;
+        bool pb_valid = false, pb_first = false, pb_last = false;
+        uint32_t pb_seg = 0;
+        bool ok = true;
+        auto issue_b = [&](uint32_t jj, uint32_t kst, uint32_t seg, bool first, bool last) -> bool {
+          if (!wait_bar(sh, PDS_FULL, jj & 1, a.status)) return false;
+          if (!wait_bar(sh, DQ_EMPTY, (jj & 1) ^ 1, a.status)) return false;
+          if (first && !wait_bar(sh, DKV_EMPTY, (seg & 1) ^ 1, a.status)) return false;
+          tc_fence_after();
+          const uint32_t qs = sb + OFF_QDO + (jj & 1) * QDO_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16(tmem + COL_DV, sdesc_sw128(qs + DO_IN_STAGE + kk * 2048, 16384, 1024),
+                      sdesc_sw128(sb + OFF_P + kk * 2048, 8192, 1024), ID_T, (kk > 0 || !first) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16(tmem + COL_DK, sdesc_sw128(qs + kk * 2048, 16384, 1024),
+                      sdesc_sw128(sb + OFF_DS + kk * 2048, 8192, 1024), ID_T, (kk > 0 || !first) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + COL_DQ, sdesc_sw128(sb + OFF_DS + kk * 32, 16, 1024),
+                      sdesc_sw128(sb + OFF_K + kst * 16384 + kk * 2048, 8192, 1024), ID_Q, kk > 0);
+          umma_commit(&sh->bar[PDS_EMPTY]);
+          umma_commit(&sh->bar[QDO_EMPTY + (jj & 1)]);
+          umma_commit(&sh->bar[DQ_FULL]);
+          if (last) {
+            umma_commit(&sh->bar[K_EMPTY + kst]);
+            umma_commit(&sh->bar[DKV_FULL]);
+          }
+          return true;
+        };
+        while (s.cur >= 0) {
+          const int t = s.cur;
+          const int64_t key = bucket_key(meta, t);
+          const bool first = key != prev;
+          if (first) ++nseg;
+          const uint32_t seg = nseg - 1, kst = seg & 1;
+          const bool last = s.nxt < 0 || bucket_key(meta, s.nxt) != key;
+          // A(j): S = Q K^T, dP = dO V^T
+          const uint32_t qst = j & 1;
+          if (!wait_bar(sh, QDO_FULL + qst, (j >> 1) & 1, a.status)) { ok = false; break; }
+          if (first && !wait_bar(sh, KV_FULL + kst, (seg >> 1) & 1, a.status)) { ok = false; break; }
+          if (!wait_bar(sh, S_EMPTY + qst, ((j >> 1) & 1) ^ 1, a.status)) { ok = false; break; }
+          tc_fence_after();
+          {
+            const uint32_t qs = sb + OFF_QDO + qst * QDO_STAGE;
+            const uint32_t ks = sb + OFF_K + kst * 16384;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32, koff = (kk >> 2) * 8192 + (kk & 3) * 32;
+              umma_bf16(tmem + col_s(qst), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + koff, 16, 1024), ID_S,
+                        kk > 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32, koff = (kk >> 2) * 8192 + (kk & 3) * 32;
+              umma_bf16(tmem + col_dp(qst), sdesc_sw128(qs + DO_IN_STAGE + off, 16, 1024),
+                        sdesc_sw128(sb + OFF_V + koff, 16, 1024), ID_S, kk > 0);
+            }
+            umma_commit(&sh->bar[S_FULL + qst]);
+            if (last) umma_commit(&sh->bar[V_EMPTY]);
+          }
+          // B(j-1)
+          if (pb_valid && !issue_b(pb_j, pb_kst, pb_seg, pb_first, pb_last)) { ok = false; break; }
+          pb_valid = true; pb_j = j; pb_kst = kst; pb_seg = seg; pb_first = first; pb_last = last;
+          prev = key;
+          ++j;
+          s.advance();
+        }
+        if (ok && pb_valid) issue_b(pb_j, pb_kst, pb_seg, pb_first, pb_last);
+      }
+    } else if (warp < kRed0) {
+      // ------------------------------------------------------------ softmax / dS
+      const int sp = warp & 3, half = (warp - kComp0) >> 2;
+      const int m = sp * 32 + lane, slot = m >> 4, hh = m & 15;
+      const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
+      Seq s;
+      s.init(a.walk);
+      uint32_t j = 0;
+      while (s.cur >= 0) {
+        const int t = s.cur;
+        const int hi = meta[(int64_t)t * MSA_TASK_META_COLS];
+        const int b = meta[(int64_t)t * MSA_TASK_META_COLS + 5];
+        const int tok0 = a.q_rows[(int64_t)t * 8];
+        const int qpos = a.q_pos[(int64_t)t * 8 + slot];
+        float lse2 = 0.f, dsc = 0.f;
+        if (qpos >= 0) {
+          const int64_t row = (int64_t)(tok0 + slot) * a.Hq + hi * 16 + hh;
+          lse2 = a.lse[row] * kLog2e;
+          dsc = a.delta[row] * a.scale;
+        }
+        const uint32_t qst = j & 1;
+        if (!wait_bar_warp(sh, S_FULL + qst, (j >> 1) & 1, a.status)) break;
+        tc_fence_after();
+        uint32_t sv[32], dpv[32];
+        tmem_ld16(tmem + lane_base + col_s(qst) + half * 32, *reinterpret_cast<uint32_t(*)[16]>(sv));
+        tmem_ld16(tmem + lane_base + col_s(qst) + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(sv + 16));
+        tmem_ld16(tmem + lane_base + col_dp(qst) + half * 32, *reinterpret_cast<uint32_t(*)[16]>(dpv));
+        tmem_ld16(tmem + lane_base + col_dp(qst) + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(dpv + 16));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->bar[S_EMPTY + qst]);
+        const int kbase = b * 64 + half * 32;
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p[2], ds[2];
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            const bool valid = kbase + e + x <= qpos;
+            const float pv = ex2_approx(fmaf(__uint_as_float(sv[e + x]), a.scale_log2, -lse2));
+            p[x] = valid ? pv : 0.f;
+            ds[x] = valid ? pv * fmaf(__uint_as_float(dpv[e + x]), a.scale, -dsc) : 0.f;
+          }
+          pk[e >> 1] = pack_bf16x2(p[0], p[1]);
+          dk[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+        }
+        if (!wait_bar_warp(sh, PDS_EMPTY, (j & 1) ^ 1, a.status)) break;
+        uint8_t* prow = sm + OFF_P + m * 128;
+        uint8_t* drow = sm + OFF_DS + m * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t o = static_cast<uint32_t>(((half * 4 + c) ^ (m & 7)) << 4);
+          *reinterpret_cast<uint4*>(prow + o) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          *reinterpret_cast<uint4*>(drow + o) = make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->bar[PDS_FULL]);
+        ++j;
+        s.advance();
+      }
+    } else {
+      // ------------------------------------------------------------ reduce
+      const int sp = warp & 3;
+      const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
+      uint8_t* stg = sm + OFF_ST + (warp - kRed0) * 4096;
+      Seq s;
+      s.init(a.walk);
+      uint32_t j = 0, nseg = 0;
+      int64_t prev = -1;
+      while (s.cur >= 0) {
+        const int t = s.cur;
+        const int64_t key = bucket_key(meta, t);
+        if (key != prev) ++nseg;
+        const bool last = s.nxt < 0 || bucket_key(meta, s.nxt) != key;
+        const int hi = meta[(int64_t)t * MSA_TASK_META_COLS];
+        const int tok0 = a.q_rows[(int64_t)t * 8];
+        if (!wait_bar_warp(sh, DQ_FULL, j & 1, a.status)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int rr = 0; rr < 4; ++rr) {
+          uint32_t v[32];
+          tmem_ld16(tmem + lane_base + COL_DQ + rr * 32, *reinterpret_cast<uint32_t(*)[16]>(v));
+          tmem_ld16(tmem + lane_base + COL_DQ + rr * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+          tmem_ld_wait();
+          if (rr == 3) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh->bar[DQ_EMPTY]);
+          }
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_3d(&tmdQ, stg, rr * 32, hi * 16, tok0 + 2 * sp);
+            bulk_commit();
+          }
+        }
+        if (last) {
+          const uint32_t seg = nseg - 1;
+          if (!wait_bar_warp(sh, DKV_FULL, seg & 1, a.status)) break;
+          tc_fence_after();
+          const int d = meta[(int64_t)t * MSA_TASK_META_COLS + 4];
+          const int b = meta[(int64_t)t * MSA_TASK_META_COLS + 5];
+          const int kvrow = a.kv_doc_starts[d] + b * 64;
+#pragma unroll 1
+          for (int q = 0; q < 4; ++q) {
+            const int which = q >> 1, kh = q & 1;
+            uint32_t v[32];
+            const uint32_t col = (which ? COL_DV : COL_DK) + kh * 32;
+            tmem_ld16(tmem + lane_base + col, *reinterpret_cast<uint32_t(*)[16]>(v));
+            tmem_ld16(tmem + lane_base + col + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+            tmem_ld_wait();
+            if (q == 3) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sh->bar[DKV_EMPTY]);
+            }
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              *reinterpret_cast<uint32_t*>(stg + e * 128 + (((lane >> 2) ^ (e & 7)) << 4) + (lane & 3) * 4) = v[e];
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_3d(which ? &tmdV : &tmdK, stg, sp * 32, hi, kvrow + kh * 32);
+              bulk_commit();
+            }
+          }
+        }
+        prev = key;
+        ++j;
+        s.advance();
+      }
+      if (lane == 0) bulk_wait_all();
+    }
+  }
+  __syncwarp();
+  // drain: make sure no MMA is still writing TMEM before it is released
+  if (warp == kMmaWarp && lane == 0) {
+    umma_commit(&sh->bar[DRAIN]);
+    wait_bar(sh, DRAIN, 0, a.status, false);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace msa
