@@ -1,13 +1,18 @@
 // Warp-specialised, pipelined main backward kernel (sm_103a).
 //
-// Roles (14 warps, 448 threads, one CTA per SM, persistent over the walk):
-//   warp 0      TMA producer: K/V once per bucket segment (K double-buffered,
+// Roles (15 warps, 480 threads, one CTA per SM, persistent over the walk):
+//   warp 0      task-info producer: walks the CTA's task sequence up to
+//               kInfo tasks ahead and publishes, per task, its index head,
+//               key block, K/V row, token row, query positions and bucket
+//               segment flags in a shared-memory ring, so no other role reads
+//               task tables from global memory on its critical path.
+//   warp 1      TMA producer: K/V once per bucket segment (K double-buffered,
 //               V single), Q/dO per task into a 2-stage ring.
-//   warp 1      MMA issuer (one lane): S/dP of task j+1 before dV/dK/dQ of
+//   warp 2      MMA issuer (one lane): S/dP of task j+1 before dV/dK/dQ of
 //               task j, so the tensor core works while task j's softmax runs.
-//   warps 2-9   softmax / dS: TMEM -> registers -> P, dS (bf16, swizzled smem).
-//               Warp w owns TMEM lanes 32*(w%4).. and key columns 32*((w-2)/4)..
-//   warps 10-13 reduce: dQ per task and dK/dV per segment, TMEM -> swizzled
+//   warps 3-10  softmax / dS: TMEM -> registers -> P, dS (bf16, swizzled smem).
+//               Warp w owns TMEM lanes 32*(w%4).. and key columns 32*((w-3)/4)..
+//   warps 11-14 reduce: dQ per task and dK/dV per segment, TMEM -> swizzled
 //               4 KB fp32 staging per warp -> TMA bulk reduce-add.
 //
 // TMEM (512 columns): S[2] at 0/128, dP[2] at 64/192, dQ at 256 (128 cols),
@@ -20,9 +25,10 @@
 namespace msa {
 namespace ws {
 
-constexpr int kWarps = 14;
+constexpr int kWarps = 15;
 constexpr int kThreads = kWarps * 32;
-constexpr int kLoadWarp = 0, kMmaWarp = 1, kComp0 = 2, kNumComp = 8, kRed0 = 10, kNumRed = 4;
+constexpr int kInfoWarp = 0, kLoadWarp = 1, kMmaWarp = 2, kComp0 = 3, kNumComp = 8, kRed0 = 11, kNumRed = 4;
+constexpr int kInfo = 8;  // task-info ring entries
 
 constexpr uint32_t OFF_QDO = 0;          // 2 stages x (Q 32 KB | dO 32 KB)
 constexpr uint32_t QDO_STAGE = 65536;
@@ -32,14 +38,24 @@ constexpr uint32_t OFF_V = 163840;       // 16 KB
 constexpr uint32_t OFF_P = 180224;       // 16 KB, [128 rows][64 keys] bf16
 constexpr uint32_t OFF_DS = 196608;      // 16 KB
 constexpr uint32_t OFF_ST = 212992;      // 4 warps x 4 KB fp32 staging
-constexpr uint32_t OFF_BAR = 229376;
-constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+constexpr uint32_t OFF_BAR = 229376;    // barriers, then the task-info ring
+constexpr uint32_t SMEM = OFF_BAR + 1024 + 1024;
 
 enum : int {
   QDO_FULL = 0, QDO_EMPTY = 2, KV_FULL = 4, K_EMPTY = 6, V_EMPTY = 8, S_FULL = 9, S_EMPTY = 11,
   PDS_FULL = 13, PDS_EMPTY = 14, DQ_FULL = 15, DQ_EMPTY = 16, DKV_FULL = 17, DKV_EMPTY = 18, DRAIN = 19,
-  NUM_BARS = 20
+  INFO_FULL = 20, INFO_EMPTY = 28, NUM_BARS = 36
 };
+
+// One task as every role needs it.
+struct TaskInfo {
+  int32_t hi, tok0, b, kvrow;
+  int32_t flags;          // bit 0: first task of its bucket segment, bit 1: last
+  uint32_t seg;           // segment ordinal within this CTA's sequence
+  int32_t pad[2];
+  int32_t qpos[8];        // document-local position of each token slot, -1 = empty
+};
+static_assert(sizeof(TaskInfo) == 64, "task info entry");
 
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_DQ = 256, COL_DK = 384, COL_DV = 448;
@@ -97,7 +113,10 @@ struct Shared {
   uint64_t bar[NUM_BARS];
   uint32_t tmem_base;
   int abort;
+  int32_t pad[14];
+  TaskInfo info[kInfo];
 };
+static_assert(sizeof(Shared) <= 1024, "shared control block");
 
 // Single-thread wait.  Gives up (false) on timeout, or as soon as another role
 // has aborted unless honor_abort is false (used for the final MMA drain).
@@ -142,9 +161,13 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    const uint32_t counts[NUM_BARS] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, kNumComp, kNumComp, kNumComp, 1,
-                                       1, kNumRed, 1, kNumRed, 1};
-    for (int i = 0; i < NUM_BARS; ++i) mbar_init(&sh->bar[i], counts[i]);
+    const uint32_t counts[INFO_FULL] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, kNumComp, kNumComp, kNumComp, 1,
+                                        1, kNumRed, 1, kNumRed, 1};
+    for (int i = 0; i < INFO_FULL; ++i) mbar_init(&sh->bar[i], counts[i]);
+    for (int i = 0; i < kInfo; ++i) {
+      mbar_init(&sh->bar[INFO_FULL + i], 1);
+      mbar_init(&sh->bar[INFO_EMPTY + i], kNumRed);
+    }
     sh->abort = 0;
     fence_mbar_init();
   }
@@ -159,49 +182,79 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
   const int32_t* meta = a.meta;
 
   if (!status_bad(a.status)) {
-    if (warp == kLoadWarp) {
-      // ------------------------------------------------------------ producer
+    if (warp == kInfoWarp) {
+      // ------------------------------------------------------------ task info
+      if (lane == 0) {
+        Seq s;
+        s.init(a.walk);
+        uint32_t j = 0, nseg = 0;
+        int64_t prev = -1;
+        int64_t key = s.cur >= 0 ? bucket_key(meta, s.cur) : -1;
+        while (s.cur >= 0) {
+          const int t = s.cur;
+          const int64_t nkey = s.nxt >= 0 ? bucket_key(meta, s.nxt) : -2;
+          const int32_t* mt = meta + (int64_t)t * MSA_TASK_META_COLS;
+          const int hi = mt[0], d = mt[4], b = mt[5];
+          const int tok0 = a.q_rows[(int64_t)t * 8];
+          const int4 qp0 = *reinterpret_cast<const int4*>(a.q_pos + (int64_t)t * 8);
+          const int4 qp1 = *reinterpret_cast<const int4*>(a.q_pos + (int64_t)t * 8 + 4);
+          const int kvrow = a.kv_doc_starts[d] + b * 64;
+          const bool first = key != prev;
+          if (first) ++nseg;
+          const uint32_t slot = j % kInfo;
+          if (!wait_bar(sh, INFO_EMPTY + slot, ((j / kInfo) & 1) ^ 1, a.status)) break;
+          TaskInfo& e = sh->info[slot];
+          e.hi = hi; e.tok0 = tok0; e.b = b; e.kvrow = kvrow;
+          e.flags = (first ? 1 : 0) | (nkey != key ? 2 : 0);
+          e.seg = nseg - 1;
+          e.qpos[0] = qp0.x; e.qpos[1] = qp0.y; e.qpos[2] = qp0.z; e.qpos[3] = qp0.w;
+          e.qpos[4] = qp1.x; e.qpos[5] = qp1.y; e.qpos[6] = qp1.z; e.qpos[7] = qp1.w;
+          mbar_arrive(&sh->bar[INFO_FULL + slot]);
+          prev = key;
+          key = nkey;
+          ++j;
+          s.advance();
+        }
+        // a sentinel entry tells every consumer that the sequence has ended
+        const uint32_t slot = j % kInfo;
+        if (wait_bar(sh, INFO_EMPTY + slot, ((j / kInfo) & 1) ^ 1, a.status)) {
+          sh->info[slot].hi = -1;
+          mbar_arrive(&sh->bar[INFO_FULL + slot]);
+        }
+      }
+    } else if (warp == kLoadWarp) {
+      // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmdO);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
-        Seq s;
-        s.init(a.walk);
-        uint32_t nq = 0, nseg = 0;
-        int64_t prev = -1;
-        while (s.cur >= 0) {
-          const int t = s.cur;
-          const int64_t key = bucket_key(meta, t);
-          const int hi = meta[(int64_t)t * MSA_TASK_META_COLS];
-          if (key != prev) {
-            const int d = meta[(int64_t)t * MSA_TASK_META_COLS + 4];
-            const int b = meta[(int64_t)t * MSA_TASK_META_COLS + 5];
-            const uint32_t kst = nseg & 1;
-            if (!wait_bar(sh, K_EMPTY + kst, ((nseg >> 1) & 1) ^ 1, a.status)) break;
-            if (!wait_bar(sh, V_EMPTY, (nseg & 1) ^ 1, a.status)) break;
-            const int kvrow = a.kv_doc_starts[d] + b * 64;
+        for (uint32_t j = 0;; ++j) {
+          const uint32_t slot = j % kInfo;
+          if (!wait_bar(sh, INFO_FULL + slot, (j / kInfo) & 1, a.status)) break;
+          const TaskInfo& e = sh->info[slot];
+          const int hi = e.hi;
+          if (hi < 0) break;
+          if (e.flags & 1) {
+            const uint32_t seg = e.seg, kst = seg & 1;
+            if (!wait_bar(sh, K_EMPTY + kst, ((seg >> 1) & 1) ^ 1, a.status)) break;
+            if (!wait_bar(sh, V_EMPTY, (seg & 1) ^ 1, a.status)) break;
             uint64_t* fb = &sh->bar[KV_FULL + kst];
             mbar_arrive_expect_tx(fb, 32768u);
-            tma_load_3d(sm + OFF_K + kst * 16384, &tmK, fb, 0, hi, kvrow);
-            tma_load_3d(sm + OFF_K + kst * 16384 + 8192, &tmK, fb, 64, hi, kvrow);
-            tma_load_3d(sm + OFF_V, &tmV, fb, 0, hi, kvrow);
-            tma_load_3d(sm + OFF_V + 8192, &tmV, fb, 64, hi, kvrow);
-            ++nseg;
-            prev = key;
+            tma_load_3d(sm + OFF_K + kst * 16384, &tmK, fb, 0, hi, e.kvrow);
+            tma_load_3d(sm + OFF_K + kst * 16384 + 8192, &tmK, fb, 64, hi, e.kvrow);
+            tma_load_3d(sm + OFF_V, &tmV, fb, 0, hi, e.kvrow);
+            tma_load_3d(sm + OFF_V + 8192, &tmV, fb, 64, hi, e.kvrow);
           }
-          const uint32_t qst = nq & 1;
-          if (!wait_bar(sh, QDO_EMPTY + qst, ((nq >> 1) & 1) ^ 1, a.status)) break;
-          const int tok0 = a.q_rows[(int64_t)t * 8];
+          const uint32_t qst = j & 1;
+          if (!wait_bar(sh, QDO_EMPTY + qst, ((j >> 1) & 1) ^ 1, a.status)) break;
           uint64_t* fb = &sh->bar[QDO_FULL + qst];
           uint8_t* st = sm + OFF_QDO + qst * QDO_STAGE;
           mbar_arrive_expect_tx(fb, 65536u);
-          tma_load_3d(st, &tmQ, fb, 0, hi * 16, tok0);
-          tma_load_3d(st + 16384, &tmQ, fb, 64, hi * 16, tok0);
-          tma_load_3d(st + DO_IN_STAGE, &tmdO, fb, 0, hi * 16, tok0);
-          tma_load_3d(st + DO_IN_STAGE + 16384, &tmdO, fb, 64, hi * 16, tok0);
-          ++nq;
-          s.advance();
+          tma_load_3d(st, &tmQ, fb, 0, hi * 16, e.tok0);
+          tma_load_3d(st + 16384, &tmQ, fb, 64, hi * 16, e.tok0);
+          tma_load_3d(st + DO_IN_STAGE, &tmdO, fb, 0, hi * 16, e.tok0);
+          tma_load_3d(st + DO_IN_STAGE + 16384, &tmdO, fb, 64, hi * 16, e.tok0);
         }
       }
     } else if (warp == kMmaWarp) {
@@ -211,14 +264,8 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         constexpr uint32_t ID_T = idesc_bf16_f32(128, 64, true, true);
         constexpr uint32_t ID_Q = idesc_bf16_f32(128, 128, false, true);
         const uint32_t sb = smem_u32(sm);
-        Seq s;
-        s.init(a.walk);
-        uint32_t j = 0, nseg = 0;
-        int64_t prev = -1;
-        // pending B: task index j-1 and its segment facts
-        uint32_t pb_j = 0, pb_kst = 0;
+        uint32_t pb_j = 0, pb_kst = 0, pb_seg = 0;
         bool pb_valid = false, pb_first = false, pb_last = false;
-        uint32_t pb_seg = 0;
         bool ok = true;
         auto issue_b = [&](uint32_t jj, uint32_t kst, uint32_t seg, bool first, bool last) -> bool {
           if (!wait_bar(sh, PDS_FULL, jj & 1, a.status)) return false;
@@ -247,13 +294,13 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           }
           return true;
         };
-        while (s.cur >= 0) {
-          const int t = s.cur;
-          const int64_t key = bucket_key(meta, t);
-          const bool first = key != prev;
-          if (first) ++nseg;
-          const uint32_t seg = nseg - 1, kst = seg & 1;
-          const bool last = s.nxt < 0 || bucket_key(meta, s.nxt) != key;
+        for (uint32_t j = 0;; ++j) {
+          const uint32_t slot = j % kInfo;
+          if (!wait_bar(sh, INFO_FULL + slot, (j / kInfo) & 1, a.status)) { ok = false; break; }
+          const TaskInfo& e = sh->info[slot];
+          if (e.hi < 0) break;
+          const bool first = e.flags & 1, last = (e.flags >> 1) & 1;
+          const uint32_t seg = e.seg, kst = seg & 1;
           // A(j): S = Q K^T, dP = dO V^T
           const uint32_t qst = j & 1;
           if (!wait_bar(sh, QDO_FULL + qst, (j >> 1) & 1, a.status)) { ok = false; break; }
@@ -281,90 +328,96 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           // B(j-1)
           if (pb_valid && !issue_b(pb_j, pb_kst, pb_seg, pb_first, pb_last)) { ok = false; break; }
           pb_valid = true; pb_j = j; pb_kst = kst; pb_seg = seg; pb_first = first; pb_last = last;
-          prev = key;
-          ++j;
-          s.advance();
         }
         if (ok && pb_valid) issue_b(pb_j, pb_kst, pb_seg, pb_first, pb_last);
       }
     } else if (warp < kRed0) {
       // ------------------------------------------------------------ softmax / dS
       const int sp = warp & 3, half = (warp - kComp0) >> 2;
-      const int m = sp * 32 + lane, slot = m >> 4, hh = m & 15;
+      const int m = sp * 32 + lane, slot_row = m >> 4, hh = m & 15;
       const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
-      Seq s;
-      s.init(a.walk);
-      uint32_t j = 0;
-      while (s.cur >= 0) {
-        const int t = s.cur;
-        const int hi = meta[(int64_t)t * MSA_TASK_META_COLS];
-        const int b = meta[(int64_t)t * MSA_TASK_META_COLS + 5];
-        const int tok0 = a.q_rows[(int64_t)t * 8];
-        const int qpos = a.q_pos[(int64_t)t * 8 + slot];
-        float lse2 = 0.f, dsc = 0.f;
+      // per-row LSE and D of the next task, loaded one task ahead
+      auto fetch = [&](const TaskInfo& e, int& qpos, float& lse2, float& dsc) {
+        qpos = e.qpos[slot_row];
+        lse2 = 0.f;
+        dsc = 0.f;
         if (qpos >= 0) {
-          const int64_t row = (int64_t)(tok0 + slot) * a.Hq + hi * 16 + hh;
+          const int64_t row = (int64_t)(e.tok0 + slot_row) * a.Hq + e.hi * 16 + hh;
           lse2 = a.lse[row] * kLog2e;
           dsc = a.delta[row] * a.scale;
         }
-        const uint32_t qst = j & 1;
-        if (!wait_bar_warp(sh, S_FULL + qst, (j >> 1) & 1, a.status)) break;
-        tc_fence_after();
-        uint32_t sv[32], dpv[32];
-        tmem_ld16(tmem + lane_base + col_s(qst) + half * 32, *reinterpret_cast<uint32_t(*)[16]>(sv));
-        tmem_ld16(tmem + lane_base + col_s(qst) + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(sv + 16));
-        tmem_ld16(tmem + lane_base + col_dp(qst) + half * 32, *reinterpret_cast<uint32_t(*)[16]>(dpv));
-        tmem_ld16(tmem + lane_base + col_dp(qst) + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(dpv + 16));
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->bar[S_EMPTY + qst]);
-        const int kbase = b * 64 + half * 32;
-        uint32_t pk[16], dk[16];
+      };
+      if (!wait_bar_warp(sh, INFO_FULL + 0, 0, a.status)) goto comp_done;
+      {
+        int qpos, nqpos = -1;
+        float lse2, dsc, nlse2 = 0.f, ndsc = 0.f;
+        int b = sh->info[0].b;
+        bool more = sh->info[0].hi >= 0;
+        if (more) fetch(sh->info[0], qpos, lse2, dsc);
+        for (uint32_t j = 0; more; ++j) {
+          // look ahead: next task's info and its per-row scalars
+          const uint32_t nslot = (j + 1) % kInfo;
+          if (!wait_bar_warp(sh, INFO_FULL + nslot, ((j + 1) / kInfo) & 1, a.status)) break;
+          const TaskInfo& ne = sh->info[nslot];
+          const bool nmore = ne.hi >= 0;
+          const int nb = ne.b;
+          if (nmore) fetch(ne, nqpos, nlse2, ndsc);
+          const uint32_t qst = j & 1;
+          if (!wait_bar_warp(sh, S_FULL + qst, (j >> 1) & 1, a.status)) break;
+          tc_fence_after();
+          uint32_t sv[32], dpv[32];
+          tmem_ld16(tmem + lane_base + col_s(qst) + half * 32, *reinterpret_cast<uint32_t(*)[16]>(sv));
+          tmem_ld16(tmem + lane_base + col_s(qst) + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(sv + 16));
+          tmem_ld16(tmem + lane_base + col_dp(qst) + half * 32, *reinterpret_cast<uint32_t(*)[16]>(dpv));
+          tmem_ld16(tmem + lane_base + col_dp(qst) + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(dpv + 16));
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->bar[S_EMPTY + qst]);
+          const int kbase = b * 64 + half * 32;
+          uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p[2], ds[2];
+          for (int e = 0; e < 32; e += 2) {
+            float p[2], ds[2];
 #pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            const bool valid = kbase + e + x <= qpos;
-            const float pv = ex2_approx(fmaf(__uint_as_float(sv[e + x]), a.scale_log2, -lse2));
-            p[x] = valid ? pv : 0.f;
-            ds[x] = valid ? pv * fmaf(__uint_as_float(dpv[e + x]), a.scale, -dsc) : 0.f;
+            for (int x = 0; x < 2; ++x) {
+              const bool valid = kbase + e + x <= qpos;
+              const float pv = ex2_approx(fmaf(__uint_as_float(sv[e + x]), a.scale_log2, -lse2));
+              p[x] = valid ? pv : 0.f;
+              ds[x] = valid ? pv * fmaf(__uint_as_float(dpv[e + x]), a.scale, -dsc) : 0.f;
+            }
+            pk[e >> 1] = pack_bf16x2(p[0], p[1]);
+            dk[e >> 1] = pack_bf16x2(ds[0], ds[1]);
           }
-          pk[e >> 1] = pack_bf16x2(p[0], p[1]);
-          dk[e >> 1] = pack_bf16x2(ds[0], ds[1]);
-        }
-        if (!wait_bar_warp(sh, PDS_EMPTY, (j & 1) ^ 1, a.status)) break;
-        uint8_t* prow = sm + OFF_P + m * 128;
-        uint8_t* drow = sm + OFF_DS + m * 128;
+          if (!wait_bar_warp(sh, PDS_EMPTY, (j & 1) ^ 1, a.status)) break;
+          uint8_t* prow = sm + OFF_P + m * 128;
+          uint8_t* drow = sm + OFF_DS + m * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t o = static_cast<uint32_t>(((half * 4 + c) ^ (m & 7)) << 4);
-          *reinterpret_cast<uint4*>(prow + o) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          *reinterpret_cast<uint4*>(drow + o) = make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t o = static_cast<uint32_t>(((half * 4 + c) ^ (m & 7)) << 4);
+            *reinterpret_cast<uint4*>(prow + o) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            *reinterpret_cast<uint4*>(drow + o) = make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->bar[PDS_FULL]);
+          qpos = nqpos; lse2 = nlse2; dsc = ndsc; b = nb; more = nmore;
         }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->bar[PDS_FULL]);
-        ++j;
-        s.advance();
       }
+    comp_done:;
     } else {
       // ------------------------------------------------------------ reduce
       const int sp = warp & 3;
       const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
       uint8_t* stg = sm + OFF_ST + (warp - kRed0) * 4096;
-      Seq s;
-      s.init(a.walk);
-      uint32_t j = 0, nseg = 0;
-      int64_t prev = -1;
-      while (s.cur >= 0) {
-        const int t = s.cur;
-        const int64_t key = bucket_key(meta, t);
-        if (key != prev) ++nseg;
-        const bool last = s.nxt < 0 || bucket_key(meta, s.nxt) != key;
-        const int hi = meta[(int64_t)t * MSA_TASK_META_COLS];
-        const int tok0 = a.q_rows[(int64_t)t * 8];
+      for (uint32_t j = 0;; ++j) {
+        const uint32_t slot = j % kInfo;
+        if (!wait_bar_warp(sh, INFO_FULL + slot, (j / kInfo) & 1, a.status)) break;
+        const TaskInfo& e = sh->info[slot];
+        const int hi = e.hi, tok0 = e.tok0, kvrow = e.kvrow, flags = e.flags;
+        const uint32_t seg = e.seg;
+        __syncwarp();
+        if (hi < 0) break;
         if (!wait_bar_warp(sh, DQ_FULL, j & 1, a.status)) break;
         tc_fence_after();
 #pragma unroll 1
@@ -391,13 +444,9 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
             bulk_commit();
           }
         }
-        if (last) {
-          const uint32_t seg = nseg - 1;
+        if (flags & 2) {
           if (!wait_bar_warp(sh, DKV_FULL, seg & 1, a.status)) break;
           tc_fence_after();
-          const int d = meta[(int64_t)t * MSA_TASK_META_COLS + 4];
-          const int b = meta[(int64_t)t * MSA_TASK_META_COLS + 5];
-          const int kvrow = a.kv_doc_starts[d] + b * 64;
 #pragma unroll 1
           for (int q = 0; q < 4; ++q) {
             const int which = q >> 1, kh = q & 1;
@@ -414,8 +463,8 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              *reinterpret_cast<uint32_t*>(stg + e * 128 + (((lane >> 2) ^ (e & 7)) << 4) + (lane & 3) * 4) = v[e];
+            for (int ee = 0; ee < 32; ++ee)
+              *reinterpret_cast<uint32_t*>(stg + ee * 128 + (((lane >> 2) ^ (ee & 7)) << 4) + (lane & 3) * 4) = v[ee];
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -424,9 +473,9 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
             }
           }
         }
-        prev = key;
-        ++j;
-        s.advance();
+        // this reduce warp is done with the task: release its info entry
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->bar[INFO_EMPTY + slot]);
       }
       if (lane == 0) bulk_wait_all();
     }
