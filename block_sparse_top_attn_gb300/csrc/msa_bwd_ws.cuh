@@ -1,6 +1,6 @@
 // Warp-specialised, pipelined main backward kernel (sm_103a).
 //
-// Roles (15 warps, 480 threads, one CTA per SM, persistent over the walk):
+// Roles (16 warps, 512 threads, one CTA per SM, persistent over the walk):
 //   warp 0      task-info producer: walks the CTA's task sequence up to
 //               kInfo tasks ahead and publishes, per task, its index head,
 //               key block, K/V row, token row, query positions and bucket
@@ -8,11 +8,14 @@
 //               task tables from global memory on its critical path.
 //   warp 1      TMA producer: K/V once per bucket segment (K double-buffered,
 //               V single), Q/dO per task into a 2-stage ring.
-//   warp 2      MMA issuer (one lane): S/dP of task j+1 before dV/dK/dQ of
-//               task j, so the tensor core works while task j's softmax runs.
-//   warps 3-10  softmax / dS: TMEM -> registers -> P, dS (bf16, swizzled smem).
-//               Warp w owns TMEM lanes 32*(w%4).. and key columns 32*((w-3)/4)..
-//   warps 11-14 reduce: dQ per task and dK/dV per segment, TMEM -> swizzled
+//   warp 2      MMA issuer A (one lane): S and dP of each task.
+//   warp 3      MMA issuer B (one lane): dK^T, dV^T and dQ of each task.  Two
+//               issuing threads keep the tensor core fed while each waits on
+//               its own dependencies; their TMEM targets are disjoint and every
+//               cross-phase ordering goes through an mbarrier.
+//   warps 4-11  softmax / dS: TMEM -> registers -> P, dS (bf16, swizzled smem).
+//               Warp w owns TMEM lanes 32*(w%4).. and key columns 32*((w-4)/4)..
+//   warps 12-15 reduce: dQ per task and dK/dV per segment, TMEM -> swizzled
 //               4 KB fp32 staging per warp -> TMA bulk reduce-add.
 //
 // TMEM (512 columns): S[2] at 0/128, dP[2] at 64/192, dQ at 256 (128 cols),
@@ -25,9 +28,10 @@
 namespace msa {
 namespace ws {
 
-constexpr int kWarps = 15;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kInfoWarp = 0, kLoadWarp = 1, kMmaWarp = 2, kComp0 = 3, kNumComp = 8, kRed0 = 11, kNumRed = 4;
+constexpr int kInfoWarp = 0, kLoadWarp = 1, kMmaWarp = 2, kMmaBWarp = 3, kComp0 = 4, kNumComp = 8, kRed0 = 12,
+              kNumRed = 4;
 constexpr int kInfo = 8;  // task-info ring entries
 
 constexpr uint32_t OFF_QDO = 0;          // 2 stages x (Q 32 KB | dO 32 KB)
@@ -42,9 +46,9 @@ constexpr uint32_t OFF_BAR = 229376;    // barriers, then the task-info ring
 constexpr uint32_t SMEM = OFF_BAR + 1024 + 1024;
 
 enum : int {
-  QDO_FULL = 0, QDO_EMPTY = 2, KV_FULL = 4, K_EMPTY = 6, V_EMPTY = 8, S_FULL = 9, S_EMPTY = 11,
+  Q_FULL = 0, Q_EMPTY = 2, KV_FULL = 4, K_EMPTY = 6, V_EMPTY = 8, S_FULL = 9, S_EMPTY = 11,
   PDS_FULL = 13, PDS_EMPTY = 14, DQ_FULL = 15, DQ_EMPTY = 16, DKV_FULL = 17, DKV_EMPTY = 18, DRAIN = 19,
-  INFO_FULL = 20, INFO_EMPTY = 28, NUM_BARS = 36
+  DO_FULL = 20, DO_EMPTY = 22, INFO_FULL = 24, INFO_EMPTY = 32, NUM_BARS = 40
 };
 
 // One task as every role needs it.
@@ -113,7 +117,7 @@ struct Shared {
   uint64_t bar[NUM_BARS];
   uint32_t tmem_base;
   int abort;
-  int32_t pad[14];
+  int32_t pad[6];
   TaskInfo info[kInfo];
 };
 static_assert(sizeof(Shared) <= 1024, "shared control block");
@@ -123,7 +127,7 @@ static_assert(sizeof(Shared) <= 1024, "shared control block");
 __device__ __forceinline__ bool wait_bar(Shared* sh, int idx, uint32_t parity, int32_t* status,
                                          bool honor_abort = true) {
   uint64_t* bar = &sh->bar[idx];
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     for (int i = 0; i < 32; ++i)
@@ -162,7 +166,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
 
   if (threadIdx.x == 0) {
     const uint32_t counts[INFO_FULL] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, kNumComp, kNumComp, kNumComp, 1,
-                                        1, kNumRed, 1, kNumRed, 1};
+                                        1, kNumRed, 1, kNumRed, 2, 1, 1, 1, 1};
     for (int i = 0; i < INFO_FULL; ++i) mbar_init(&sh->bar[i], counts[i]);
     for (int i = 0; i < kInfo; ++i) {
       mbar_init(&sh->bar[INFO_FULL + i], 1);
@@ -246,90 +250,102 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
             tma_load_3d(sm + OFF_V, &tmV, fb, 0, hi, e.kvrow);
             tma_load_3d(sm + OFF_V + 8192, &tmV, fb, 64, hi, e.kvrow);
           }
-          const uint32_t qst = j & 1;
-          if (!wait_bar(sh, QDO_EMPTY + qst, ((j >> 1) & 1) ^ 1, a.status)) break;
-          uint64_t* fb = &sh->bar[QDO_FULL + qst];
+          const uint32_t qst = j & 1, qph = ((j >> 1) & 1) ^ 1;
           uint8_t* st = sm + OFF_QDO + qst * QDO_STAGE;
-          mbar_arrive_expect_tx(fb, 65536u);
-          tma_load_3d(st, &tmQ, fb, 0, hi * 16, e.tok0);
-          tma_load_3d(st + 16384, &tmQ, fb, 64, hi * 16, e.tok0);
-          tma_load_3d(st + DO_IN_STAGE, &tmdO, fb, 0, hi * 16, e.tok0);
-          tma_load_3d(st + DO_IN_STAGE + 16384, &tmdO, fb, 64, hi * 16, e.tok0);
+          if (!wait_bar(sh, Q_EMPTY + qst, qph, a.status)) break;
+          mbar_arrive_expect_tx(&sh->bar[Q_FULL + qst], 32768u);
+          tma_load_3d(st, &tmQ, &sh->bar[Q_FULL + qst], 0, hi * 16, e.tok0);
+          tma_load_3d(st + 16384, &tmQ, &sh->bar[Q_FULL + qst], 64, hi * 16, e.tok0);
+          if (!wait_bar(sh, DO_EMPTY + qst, qph, a.status)) break;
+          mbar_arrive_expect_tx(&sh->bar[DO_FULL + qst], 32768u);
+          tma_load_3d(st + DO_IN_STAGE, &tmdO, &sh->bar[DO_FULL + qst], 0, hi * 16, e.tok0);
+          tma_load_3d(st + DO_IN_STAGE + 16384, &tmdO, &sh->bar[DO_FULL + qst], 64, hi * 16, e.tok0);
+          // warm L2 with the query tiles of the task two ahead, if its info is published
+          const uint32_t ps = (j + 2) % kInfo;
+          if (mbar_test_wait(&sh->bar[INFO_FULL + ps], ((j + 2) / kInfo) & 1)) {
+            const TaskInfo& f = sh->info[ps];
+            if (f.hi >= 0) {
+              tma_prefetch_l2_3d(&tmQ, 0, f.hi * 16, f.tok0);
+              tma_prefetch_l2_3d(&tmQ, 64, f.hi * 16, f.tok0);
+              tma_prefetch_l2_3d(&tmdO, 0, f.hi * 16, f.tok0);
+              tma_prefetch_l2_3d(&tmdO, 64, f.hi * 16, f.tok0);
+            }
+          }
         }
       }
-    } else if (warp == kMmaWarp) {
-      // ------------------------------------------------------------ MMA issuer
+    } else if (warp == kMmaWarp || warp == kMmaBWarp) {
+      // ------------------------------------------------------------ MMA issuers
       if (lane == 0) {
         constexpr uint32_t ID_S = idesc_bf16_f32(128, 64, false, false);
         constexpr uint32_t ID_T = idesc_bf16_f32(128, 64, true, true);
         constexpr uint32_t ID_Q = idesc_bf16_f32(128, 128, false, true);
         const uint32_t sb = smem_u32(sm);
-        uint32_t pb_j = 0, pb_kst = 0, pb_seg = 0;
-        bool pb_valid = false, pb_first = false, pb_last = false;
-        bool ok = true;
-        auto issue_b = [&](uint32_t jj, uint32_t kst, uint32_t seg, bool first, bool last) -> bool {
-          if (!wait_bar(sh, PDS_FULL, jj & 1, a.status)) return false;
-          if (!wait_bar(sh, DQ_EMPTY, (jj & 1) ^ 1, a.status)) return false;
-          if (first && !wait_bar(sh, DKV_EMPTY, (seg & 1) ^ 1, a.status)) return false;
-          tc_fence_after();
-          const uint32_t qs = sb + OFF_QDO + (jj & 1) * QDO_STAGE;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16(tmem + COL_DV, sdesc_sw128(qs + DO_IN_STAGE + kk * 2048, 16384, 1024),
-                      sdesc_sw128(sb + OFF_P + kk * 2048, 8192, 1024), ID_T, (kk > 0 || !first) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16(tmem + COL_DK, sdesc_sw128(qs + kk * 2048, 16384, 1024),
-                      sdesc_sw128(sb + OFF_DS + kk * 2048, 8192, 1024), ID_T, (kk > 0 || !first) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + COL_DQ, sdesc_sw128(sb + OFF_DS + kk * 32, 16, 1024),
-                      sdesc_sw128(sb + OFF_K + kst * 16384 + kk * 2048, 8192, 1024), ID_Q, kk > 0);
-          umma_commit(&sh->bar[PDS_EMPTY]);
-          umma_commit(&sh->bar[QDO_EMPTY + (jj & 1)]);
-          umma_commit(&sh->bar[DQ_FULL]);
-          if (last) {
-            umma_commit(&sh->bar[K_EMPTY + kst]);
-            umma_commit(&sh->bar[DKV_FULL]);
-          }
-          return true;
-        };
+        // Descriptor bases; a K step or a stage is an immediate added to the
+        // 14-bit start-address field (byte offset >> 4; all addresses < 256 KB).
+        constexpr uint64_t kStageQ = QDO_STAGE >> 4, kStageK = 16384 >> 4;
+        const bool is_a = warp == kMmaWarp;
         for (uint32_t j = 0;; ++j) {
           const uint32_t slot = j % kInfo;
-          if (!wait_bar(sh, INFO_FULL + slot, (j / kInfo) & 1, a.status)) { ok = false; break; }
+          if (!wait_bar(sh, INFO_FULL + slot, (j / kInfo) & 1, a.status)) break;
           const TaskInfo& e = sh->info[slot];
           if (e.hi < 0) break;
           const bool first = e.flags & 1, last = (e.flags >> 1) & 1;
           const uint32_t seg = e.seg, kst = seg & 1;
-          // A(j): S = Q K^T, dP = dO V^T
-          const uint32_t qst = j & 1;
-          if (!wait_bar(sh, QDO_FULL + qst, (j >> 1) & 1, a.status)) { ok = false; break; }
-          if (first && !wait_bar(sh, KV_FULL + kst, (seg >> 1) & 1, a.status)) { ok = false; break; }
-          if (!wait_bar(sh, S_EMPTY + qst, ((j >> 1) & 1) ^ 1, a.status)) { ok = false; break; }
-          tc_fence_after();
-          {
-            const uint32_t qs = sb + OFF_QDO + qst * QDO_STAGE;
-            const uint32_t ks = sb + OFF_K + kst * 16384;
+          const uint32_t st = j & 1, ph = (j >> 1) & 1;
+          if (is_a) {
+            // S = Q K^T, dP = dO V^T.  All dependencies are polled first and the 16
+            // MMAs then go out as one burst: any shared-memory access by the issuing
+            // thread between MMAs stalls the tensor core while it drains.
+            if (first && !wait_bar(sh, KV_FULL + kst, (seg >> 1) & 1, a.status)) break;
+            if (!wait_bar(sh, S_EMPTY + st, ph ^ 1, a.status)) break;
+            if (!wait_bar(sh, Q_FULL + st, ph, a.status)) break;
+            if (!wait_bar(sh, DO_FULL + st, ph, a.status)) break;
+            tc_fence_after();
+            const uint64_t qk = sdesc_sw128(sb + OFF_QDO, 16, 1024) + st * kStageQ;
+            const uint64_t kk0 = sdesc_sw128(sb + OFF_K, 16, 1024) + kst * kStageK;
+            const uint64_t dok = sdesc_sw128(sb + OFF_QDO + DO_IN_STAGE, 16, 1024) + st * kStageQ;
+            const uint64_t vk = sdesc_sw128(sb + OFF_V, 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32, koff = (kk >> 2) * 8192 + (kk & 3) * 32;
-              umma_bf16(tmem + col_s(qst), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + koff, 16, 1024), ID_S,
-                        kk > 0);
-            }
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16(tmem + col_s(st), qk + (kk >> 2) * 1024 + (kk & 3) * 2, kk0 + (kk >> 2) * 512 + (kk & 3) * 2,
+                        ID_S, kk > 0);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32, koff = (kk >> 2) * 8192 + (kk & 3) * 32;
-              umma_bf16(tmem + col_dp(qst), sdesc_sw128(qs + DO_IN_STAGE + off, 16, 1024),
-                        sdesc_sw128(sb + OFF_V + koff, 16, 1024), ID_S, kk > 0);
-            }
-            umma_commit(&sh->bar[S_FULL + qst]);
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16(tmem + col_dp(st), dok + (kk >> 2) * 1024 + (kk & 3) * 2, vk + (kk >> 2) * 512 + (kk & 3) * 2,
+                        ID_S, kk > 0);
+            umma_commit(&sh->bar[S_FULL + st]);
             if (last) umma_commit(&sh->bar[V_EMPTY]);
+          } else {
+            // dK^T += Q^T dS, dV^T += dO^T P, dQ = dS K, as one burst of 20 MMAs
+            if (!wait_bar(sh, PDS_FULL, j & 1, a.status)) break;
+            if (first && !wait_bar(sh, DKV_EMPTY, (seg & 1) ^ 1, a.status)) break;
+            if (!wait_bar(sh, DQ_EMPTY, (j & 1) ^ 1, a.status)) break;
+            tc_fence_after();
+            const uint32_t acc0 = first ? 0u : 1u;
+            const uint64_t qm = sdesc_sw128(sb + OFF_QDO, 16384, 1024) + st * kStageQ;
+            const uint64_t dsm = sdesc_sw128(sb + OFF_DS, 8192, 1024);
+            const uint64_t dom = sdesc_sw128(sb + OFF_QDO + DO_IN_STAGE, 16384, 1024) + st * kStageQ;
+            const uint64_t pm = sdesc_sw128(sb + OFF_P, 8192, 1024);
+            const uint64_t dsk = sdesc_sw128(sb + OFF_DS, 16, 1024);
+            const uint64_t km = sdesc_sw128(sb + OFF_K, 8192, 1024) + kst * kStageK;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16(tmem + COL_DK, qm + kk * 128, dsm + kk * 128, ID_T, kk > 0 ? 1u : acc0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16(tmem + COL_DV, dom + kk * 128, pm + kk * 128, ID_T, kk > 0 ? 1u : acc0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + COL_DQ, dsk + kk * 2, km + kk * 128, ID_Q, kk > 0);
+            umma_commit(&sh->bar[Q_EMPTY + st]);
+            umma_commit(&sh->bar[DO_EMPTY + st]);
+            umma_commit(&sh->bar[PDS_EMPTY]);
+            umma_commit(&sh->bar[DQ_FULL]);
+            if (last) {
+              umma_commit(&sh->bar[K_EMPTY + kst]);
+              umma_commit(&sh->bar[DKV_FULL]);
+            }
           }
-          // B(j-1)
-          if (pb_valid && !issue_b(pb_j, pb_kst, pb_seg, pb_first, pb_last)) { ok = false; break; }
-          pb_valid = true; pb_j = j; pb_kst = kst; pb_seg = seg; pb_first = first; pb_last = last;
         }
-        if (ok && pb_valid) issue_b(pb_j, pb_kst, pb_seg, pb_first, pb_last);
       }
     } else if (warp < kRed0) {
       // ------------------------------------------------------------ softmax / dS
@@ -421,27 +437,32 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         if (!wait_bar_warp(sh, DQ_FULL, j & 1, a.status)) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int rr = 0; rr < 4; ++rr) {
-          uint32_t v[32];
-          tmem_ld16(tmem + lane_base + COL_DQ + rr * 32, *reinterpret_cast<uint32_t(*)[16]>(v));
-          tmem_ld16(tmem + lane_base + COL_DQ + rr * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t v[64];
+          tmem_ld16(tmem + lane_base + COL_DQ + hf * 64, *reinterpret_cast<uint32_t(*)[16]>(v));
+          tmem_ld16(tmem + lane_base + COL_DQ + hf * 64 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+          tmem_ld16(tmem + lane_base + COL_DQ + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[16]>(v + 32));
+          tmem_ld16(tmem + lane_base + COL_DQ + hf * 64 + 48, *reinterpret_cast<uint32_t(*)[16]>(v + 48));
           tmem_ld_wait();
-          if (rr == 3) {
+          if (hf == 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh->bar[DQ_EMPTY]);
           }
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_reduce_add_3d(&tmdQ, stg, rr * 32, hi * 16, tok0 + 2 * sp);
-            bulk_commit();
+          for (int q2 = 0; q2 < 2; ++q2) {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                  make_uint4(v[q2 * 32 + 4 * c], v[q2 * 32 + 4 * c + 1], v[q2 * 32 + 4 * c + 2], v[q2 * 32 + 4 * c + 3]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_3d(&tmdQ, stg, hf * 64 + q2 * 32, hi * 16, tok0 + 2 * sp);
+              bulk_commit();
+            }
           }
         }
         if (flags & 2) {
@@ -482,7 +503,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
   }
   __syncwarp();
   // drain: make sure no MMA is still writing TMEM before it is released
-  if (warp == kMmaWarp && lane == 0) {
+  if ((warp == kMmaWarp || warp == kMmaBWarp) && lane == 0) {
     umma_commit(&sh->bar[DRAIN]);
     wait_bar(sh, DRAIN, 0, a.status, false);
   }

@@ -56,10 +56,23 @@ MSA_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of the same condition (cheap when the phase is complete;
+// try_wait is kept for the slow path, where it may suspend the thread).
+MSA_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase with the given parity to complete.  Returns false (and
 // records MSA_ERR_TIMEOUT) if it has not completed after kWaitLimitNs.
 MSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
@@ -83,6 +96,13 @@ MSA_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+// Warm L2 with a tile (no shared memory written, no completion to wait for).
+MSA_DEV void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
 }
 MSA_DEV void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
   asm volatile(
