@@ -188,11 +188,22 @@ def _host_values(pb):
 # ---------------------------------------------------------------------------
 # GPU leg
 # ---------------------------------------------------------------------------
+MAIN_KERNEL_SOURCES = ("msa_bwd.cu", "msa_bwd_ws.cuh", "msa_common.cuh")
+
+
+def kernel_source_sha1() -> str:
+    """SHA-1 over the sources the main backward kernel is compiled from."""
+    h = hashlib.sha1()
+    for name in MAIN_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "block_sparse_top_attn_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def _traffic_record():
     """Per-launch DRAM bytes of the main kernel from the committed ncu summary,
     valid only while the kernel source it was taken on is unchanged."""
-    src = os.path.join(ROOT, "block_sparse_top_attn_gb300", "csrc", "msa_bwd.cu")
-    sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    sha = kernel_source_sha1()
     path = os.path.join(ROOT, "profiles", "bwd_main_long128k.md")
     if not os.path.exists(path):
         return None

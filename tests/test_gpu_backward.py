@@ -87,25 +87,38 @@ def test_backward_full_oracle_large(B, name):
 @pytest.mark.slow
 def test_backward_long128k_sampled(B):
     """Full-size long-context workload in the launch configuration the bench
-    times; O and LSE come from msa_fwd on the device, the oracle recomputes its
-    own O/LSE for the sampled rows, so nothing flows from the device into it."""
+    times.  The backward takes O and LSE as inputs: msa_fwd supplies them for
+    every row, then every (index head, chunk) that feeds a sampled output gets
+    the oracle's own stored-rounded O and LSE instead, so both sides
+    differentiate at the same point and nothing flows from the device into the
+    oracle."""
     import torch
     pb = W.make_problem("long128k")
     prob, t = upload(pb)
     o, lse, st = B.forward(prob, t["sel"], t["q"], t["k"], t["v"])
+    torch.cuda.synchronize()
+    assert int(st[0].item()) == 0
+    lay = O.DocLayout(pb.cu_seqlens, pb.block, pb.chunk)
+    G = pb.num_q_heads // pb.sel.shape[0]
+    rng = np.random.default_rng(0)
+    qpicks = [(0, int(rng.integers(0, 8)), int(c)) for c in rng.integers(0, lay.NC, size=12)] + [(0, 3, 0), (0, 7, lay.NC - 1)]
+    kpicks = [(0, 0, 0), (0, 5, int(lay.nb[0]) - 1), (0, 2, 1000), (0, int(rng.integers(0, 8)), int(rng.integers(0, 2048)))]
+    units = {(hi, c) for _, hi, c in qpicks}
+    for _, hi, b in kpicks:                 # one document: global chunk = local chunk
+        units |= {(hi, int(c)) for c in np.nonzero((pb.sel[hi] == b).any(axis=1))[0]}
+    for hi, c in sorted(units):
+        qp, oc, lc = O.chunk_forward(pb.q, pb.k, pb.v, lay, pb.kv_doc_starts, pb.sel, hi, 0, c, G, pb.softmax_scale)
+        rows = torch.from_numpy(int(lay.cu[0]) + qp).cuda()
+        o[rows, hi * G:(hi + 1) * G] = to_bf16_tensor(O.f64_to_bf16(oc.transpose(1, 0, 2)), "cuda")
+        lse[rows, hi * G:(hi + 1) * G] = torch.from_numpy(np.ascontiguousarray(lc.T).astype(np.float32)).cuda()
     bw = B.Backward(prob, task_tile_chunks=512)
     dq, dk, dv = bw.run(t["sel"], t["q"], t["k"], t["v"], o, t["do"], lse)
     torch.cuda.synchronize()
-    assert int(st[0].item()) == 0
     bw.check_status()
-    lay = O.DocLayout(pb.cu_seqlens, pb.block, pb.chunk)
-    rng = np.random.default_rng(0)
-    picks = [(0, int(rng.integers(0, 8)), int(c)) for c in rng.integers(0, lay.NC, size=12)] + [(0, 3, 0), (0, 7, lay.NC - 1)]
     dq_h = from_bf16_tensor(dq)
     for rows, hs, ref in O.sampled_query_grads(pb.q, pb.k, pb.v, pb.do, pb.cu_seqlens, pb.kv_doc_starts, pb.sel,
-                                               pb.block, pb.chunk, pb.softmax_scale, picks):
+                                               pb.block, pb.chunk, pb.softmax_scale, qpicks):
         assert_grad_close("dq", dq_h[rows][:, hs], ref)
-    kpicks = [(0, 0, 0), (0, 5, int(lay.nb[0]) - 1), (0, 2, 1000), (0, int(rng.integers(0, 8)), int(rng.integers(0, 2048)))]
     dk_h, dv_h = from_bf16_tensor(dk), from_bf16_tensor(dv)
     for rows, hi, gk, gv in O.sampled_key_grads(pb.q, pb.k, pb.v, pb.do, pb.cu_seqlens, pb.kv_doc_starts, pb.sel,
                                                 pb.block, pb.chunk, pb.softmax_scale, kpicks):
