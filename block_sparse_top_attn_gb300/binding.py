@@ -25,6 +25,8 @@ MSA_ERR_INVALID_SELECTION = 5
 MSA_ERR_TIMEOUT = 6
 MSA_ERR_CUDA = 7
 MSA_ERR_INVALID_DOCUMENTS = 8
+MSA_ERR_SCRATCH_TOO_SMALL = 9
+MSA_NOALLOC_SCRATCH_BYTES = 16 << 20
 MSA_TASK_META_COLS = 6
 MSA_STAGE_PREPROCESS, MSA_STAGE_MAIN, MSA_STAGE_POSTPROCESS, MSA_STAGE_ALL = 1, 2, 4, 7
 MSA_WALK_LEN = 8
@@ -68,6 +70,7 @@ def _load():
     sig = {
         "msa_workspace_bytes": (sz, [P, i64, i64, i32]),
         "msa_build_k2q": (ctypes.c_int, [P, vp, vp, vp, i64, vp, vp, sz, vp]),
+        "msa_build_k2q_noalloc": (ctypes.c_int, [P, vp, vp, vp, i64, vp, vp]),
         "msa_build_tasks": (ctypes.c_int, [P, vp, vp, i64, i32, vp, vp, vp, vp, i64, i32, vp, vp, sz, vp]),
         "msa_bwd": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, sz, vp]),
         "msa_bwd_staged": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, sz, vp,
@@ -233,6 +236,15 @@ def msa_build_k2q(p: Problem, sel, row_ptr, q_indices, edge_cap, d_status, ws, s
     _check(lib.msa_build_k2q(ctypes.byref(s), _ptr(sel), _ptr(row_ptr), _ptr(q_indices), int(edge_cap),
                              _ptr(d_status), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "msa_build_k2q")
+
+
+def msa_build_k2q_noalloc(p: Problem, sel, row_ptr, q_indices, edge_cap, d_status, stream=None):
+    """msa_build_k2q without a caller workspace: the library's fixed scratch
+    array stands in for it, for callers that may not allocate device memory."""
+    s = p.c_struct()
+    _check(lib.msa_build_k2q_noalloc(ctypes.byref(s), _ptr(sel), _ptr(row_ptr), _ptr(q_indices), int(edge_cap),
+                                     _ptr(d_status), _stream(stream)),
+           "msa_build_k2q_noalloc")
 
 
 def msa_build_tasks(p: Problem, row_ptr, q_indices, edge_cap, task_tile_chunks, task_meta, task_q_rows,

@@ -506,6 +506,35 @@ __global__ void __launch_bounds__(256) task_emit_kernel(TaskArgs a) {
   }
 }
 
+// Scratch of msa_build_k2q_noalloc, for callers that may not allocate device
+// memory.  Every device that loads the library holds one copy until exit.  In
+// host code the name is only a host-side stand-in for the symbol, so the
+// device address is looked up once per device and kept.
+static __device__ __align__(256) uint8_t g_k2q_scratch[MSA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+void* g_k2q_scratch_addr[kMaxDevices];
+std::mutex g_k2q_scratch_mu;
+
+// Device address of g_k2q_scratch on the current device.
+int k2q_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MSA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MSA_ERR_INVALID_ARGUMENT;
+  std::lock_guard<std::mutex> lk(g_k2q_scratch_mu);
+  if (!g_k2q_scratch_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_k2q_scratch) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return MSA_ERR_CUDA;
+    }
+    g_k2q_scratch_addr[dev] = ptr;
+  }
+  *out = g_k2q_scratch_addr[dev];
+  return MSA_OK;
+}
+}  // namespace
+
 }  // namespace msa
 
 using namespace msa;
@@ -526,6 +555,7 @@ const char* msa_status_string(int s) {
     case MSA_ERR_TIMEOUT: return "device wait timed out";
     case MSA_ERR_CUDA: return "CUDA error";
     case MSA_ERR_INVALID_DOCUMENTS: return "inconsistent document offsets";
+    case MSA_ERR_SCRATCH_TOO_SMALL: return "problem needs more scratch than the fixed no-allocation array holds";
     default: return "unknown status";
   }
 }
@@ -622,6 +652,18 @@ int msa_build_k2q(const msa_problem* p, const int32_t* sel, int32_t* row_ptr, in
   k2q_row_ptr_kernel<<<Hi, 1024, 0, st>>>(a);
   k2q_scatter_kernel<<<dim3((unsigned)nS, Hi), 32, hist_bytes, st>>>(a);
   return cuda_status(cudaGetLastError());
+}
+
+// Same build as msa_build_k2q with g_k2q_scratch as its workspace.
+int msa_build_k2q_noalloc(const msa_problem* p, const int32_t* sel, int32_t* row_ptr, int32_t* q_indices,
+                          int64_t edge_cap, int32_t* d_status, void* stream) {
+  int rc = check_problem(p);
+  if (rc) return rc;
+  if (k2q_ws_bytes(p) > MSA_NOALLOC_SCRATCH_BYTES) return MSA_ERR_SCRATCH_TOO_SMALL;
+  if ((rc = check_device_current())) return rc;
+  void* scratch = nullptr;
+  if ((rc = k2q_scratch_address(&scratch))) return rc;
+  return msa_build_k2q(p, sel, row_ptr, q_indices, edge_cap, d_status, scratch, MSA_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 int msa_build_tasks(const msa_problem* p, const int32_t* row_ptr, const int32_t* q_indices, int64_t edge_cap,

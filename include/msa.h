@@ -49,7 +49,8 @@ enum {
   MSA_ERR_INVALID_SELECTION = 5,  /* sel entry out of range, non-causal or repeated      */
   MSA_ERR_TIMEOUT = 6,            /* a bounded device wait expired                       */
   MSA_ERR_CUDA = 7,               /* a CUDA launch or runtime call failed                */
-  MSA_ERR_INVALID_DOCUMENTS = 8   /* cu_seqlens / kv_doc_starts inconsistent (device)    */
+  MSA_ERR_INVALID_DOCUMENTS = 8,  /* cu_seqlens / kv_doc_starts inconsistent (device)    */
+  MSA_ERR_SCRATCH_TOO_SMALL = 9   /* problem exceeds the no-allocation scratch array     */
 };
 
 /* Problem description.  Mirrors run_backward's tensor contract
@@ -132,6 +133,33 @@ size_t msa_workspace_bytes(const msa_problem* p, int64_t edge_cap, int64_t task_
  */
 int msa_build_k2q(const msa_problem* p, const int32_t* sel, int32_t* row_ptr, int32_t* q_indices,
                   int64_t edge_cap, int32_t* d_status, void* ws, size_t ws_bytes, void* stream);
+
+/* msa_build_k2q for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this entry point exists for library users, not for the
+ * method.  Some callers may not call cudaMalloc at all: a host framework whose
+ * caching allocator or fixed memory pool owns all device memory, or a latency-
+ * sensitive path that cannot afford cudaMalloc's implicit synchronisation.
+ * They still pass sel, row_ptr, q_indices and d_status, exactly as for
+ * msa_build_k2q; the build's scratch (document offsets, per-group counts and
+ * row totals) lives in one array of MSA_NOALLOC_SCRATCH_BYTES that the library
+ * holds on every GPU that loads it, until the process exits.
+ *  - The scratch a problem needs is about 8 (N+1) + 4 Hi NB (G+1) bytes, with
+ *    G = ceil(NC / S) scatter groups of S = max(64, ceil(NC / 128)) query
+ *    chunks (so G <= 128); a problem needing more is rejected with
+ *    MSA_ERR_SCRATCH_TOO_SMALL before anything is launched.  One document of
+ *    131,072 tokens with 8 index heads needs about 8.5 MB.
+ *  - The first call on a device looks up the array's device address (a
+ *    runtime query made once per device, with that device current); make that
+ *    first call before any stream capture begins.
+ *  - Every call uses the same array and it keeps what the last call left
+ *    there; the build overwrites all of it before reading, so nothing in it
+ *    needs to start at zero.  Calls whose kernels overlap on the GPU (other
+ *    streams, other host threads) race on the array and must be serialised by
+ *    the caller.
+ * It allocates nothing and returns the same codes as msa_build_k2q. */
+#define MSA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int msa_build_k2q_noalloc(const msa_problem* p, const int32_t* sel, int32_t* row_ptr,
+                          int32_t* q_indices, int64_t edge_cap, int32_t* d_status, void* stream);
 
 /* Task rows and CTA walk of the KV-parallel backward ("msa_backward_sm100"
  * page, module docstring: task rows of 8 queries x 16 heads bucketed by

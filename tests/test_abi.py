@@ -38,11 +38,11 @@ def test_header_constants_match_binding(B):
     src = open(os.path.join(ROOT, "include", "msa.h")).read()
     for name in ("MSA_OK", "MSA_ERR_INVALID_ARGUMENT", "MSA_ERR_UNSUPPORTED_DEVICE", "MSA_ERR_UNSUPPORTED_SHAPE",
                  "MSA_ERR_CAPACITY", "MSA_ERR_INVALID_SELECTION", "MSA_ERR_TIMEOUT", "MSA_ERR_CUDA",
-                 "MSA_ERR_INVALID_DOCUMENTS", "MSA_TASK_META_COLS", "MSA_WALK_LEN", "MSA_STAGE_PREPROCESS",
-                 "MSA_STAGE_MAIN", "MSA_STAGE_POSTPROCESS", "MSA_STAGE_ALL"):
+                 "MSA_ERR_INVALID_DOCUMENTS", "MSA_ERR_SCRATCH_TOO_SMALL", "MSA_TASK_META_COLS", "MSA_WALK_LEN",
+                 "MSA_STAGE_PREPROCESS", "MSA_STAGE_MAIN", "MSA_STAGE_POSTPROCESS", "MSA_STAGE_ALL"):
         m = re.search(rf"\b{name}\s*=\s*(\d+)", src)
         assert m and int(m.group(1)) == getattr(B, name), name
-    for code in range(9):
+    for code in range(10):
         assert B.status_string(code) and B.status_string(code) != "unknown status"
     assert B.status_string(99) == "unknown status"
 
