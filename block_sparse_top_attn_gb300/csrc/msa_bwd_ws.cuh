@@ -6,19 +6,32 @@
 //               key block, K/V row, token row, query positions and bucket
 //               segment flags in a shared-memory ring, so no other role reads
 //               task tables from global memory on its critical path.
-//   warp 1      TMA producer: K/V once per bucket segment (K double-buffered,
-//               V single), Q/dO per task into a 2-stage ring.
-//   warp 2      MMA issuer A (one lane): S and dP of each task.
-//   warp 3      MMA issuer B (one lane): dK^T, dV^T and dQ of each task.  Two
-//               issuing threads keep the tensor core fed while each waits on
-//               its own dependencies; their TMEM targets are disjoint and every
-//               cross-phase ordering goes through an mbarrier.
-//   warps 4-11  softmax / dS: TMEM -> registers -> P, dS (bf16, swizzled smem).
-//               Warp w owns TMEM lanes 32*(w%4).. and key columns 32*((w-4)/4)..
+//   warp 1      TMA producer: K/V once per bucket segment, Q/dO per task into
+//               a 2-stage ring.
+//   warp 2      MMA issuer A: S = Q K^T and dP = dO V^T.
+//   warp 3      MMA issuer B: dV^T += dO^T P, dK^T += Q^T dS and
+//               dQ = dS K.  Two issuing threads keep the tensor core fed while
+//               each waits on its own dependencies; their TMEM targets are
+//               disjoint and every cross-phase ordering goes through an
+//               mbarrier.
+//   warps 4-11  softmax / dS: TMEM -> registers -> P, dS (bf16, swizzled
+//               shared memory).  Warp w owns TMEM lanes 32*(w%4).. and key
+//               columns 32*((w-4)/4)..
 //   warps 12-15 reduce: dQ per task and dK/dV per segment, TMEM -> swizzled
-//               4 KB fp32 staging per warp -> TMA bulk reduce-add.
+//               fp32 staging (two 4 KB slots per warp, so a slot is refilled
+//               while the reduce-add of the other is still reading) -> TMA
+//               bulk reduce-add.
 //
-// TMEM (512 columns): S[2] at 0/128, dP[2] at 64/192, dQ at 256 (128 cols),
+// MMAs that accumulate into the same TMEM tile issue back to back only at
+// that tile's accumulate latency (about twice the issue interval of
+// independent MMAs at N = 64), so each issuer interleaves its GEMMs K step by
+// K step: S with dP, and dV^T with dK^T and dQ.
+//
+// A task's Q/dO stage is held from its TMA load until its last MMA.  dQ is
+// double-buffered in TMEM, so the dQ MMAs of task j+1 never wait for the
+// drain of task j.
+//
+// TMEM (512 columns): S at 0, dP at 64, dQ[2] at 128/256 (128 cols each),
 // dK^T at 384, dV^T at 448 (64 cols each; lane = head-dim index).
 //
 // Every mbarrier wait is bounded (kWaitLimitNs) and also gives up when any
@@ -37,18 +50,18 @@ constexpr int kInfo = 8;  // task-info ring entries
 constexpr uint32_t OFF_QDO = 0;          // 2 stages x (Q 32 KB | dO 32 KB)
 constexpr uint32_t QDO_STAGE = 65536;
 constexpr uint32_t DO_IN_STAGE = 32768;
-constexpr uint32_t OFF_K = 131072;       // 2 stages x 16 KB
-constexpr uint32_t OFF_V = 163840;       // 16 KB
-constexpr uint32_t OFF_P = 180224;       // 16 KB, [128 rows][64 keys] bf16
-constexpr uint32_t OFF_DS = 196608;      // 16 KB
-constexpr uint32_t OFF_ST = 212992;      // 4 warps x 4 KB fp32 staging
+constexpr uint32_t OFF_K = 131072;       // 16 KB, [64 keys][128 dims] bf16 (two 64-dim halves)
+constexpr uint32_t OFF_V = 147456;       // 16 KB
+constexpr uint32_t OFF_P = 163840;       // 16 KB, [128 rows][64 keys] bf16
+constexpr uint32_t OFF_DS = 180224;      // 16 KB
+constexpr uint32_t OFF_ST = 196608;      // 4 warps x 2 slots x 4 KB fp32 staging
 constexpr uint32_t OFF_BAR = 229376;    // barriers, then the task-info ring
 constexpr uint32_t SMEM = OFF_BAR + 1024 + 1024;
 
 enum : int {
-  Q_FULL = 0, Q_EMPTY = 2, KV_FULL = 4, K_EMPTY = 6, V_EMPTY = 8, S_FULL = 9, S_EMPTY = 11,
-  PDS_FULL = 13, PDS_EMPTY = 14, DQ_FULL = 15, DQ_EMPTY = 16, DKV_FULL = 17, DKV_EMPTY = 18, DRAIN = 19,
-  DO_FULL = 20, DO_EMPTY = 22, INFO_FULL = 24, INFO_EMPTY = 32, NUM_BARS = 40
+  Q_FULL = 0, Q_EMPTY = 2, DO_FULL = 4, DO_EMPTY = 6, KV_FULL = 8, K_EMPTY = 9, V_EMPTY = 10, S_FULL = 11,
+  S_EMPTY = 12, PDS_FULL = 13, PDS_EMPTY = 14, DQ_FULL = 15, DQ_EMPTY = 17, DKV_FULL = 19, DKV_EMPTY = 20,
+  DRAIN = 21, INFO_FULL = 22, INFO_EMPTY = INFO_FULL + kInfo, NUM_BARS = INFO_EMPTY + kInfo
 };
 
 // One task as every role needs it.
@@ -62,9 +75,8 @@ struct TaskInfo {
 static_assert(sizeof(TaskInfo) == 64, "task info entry");
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_DQ = 256, COL_DK = 384, COL_DV = 448;
-__device__ __forceinline__ uint32_t col_s(uint32_t st) { return st * 128; }
-__device__ __forceinline__ uint32_t col_dp(uint32_t st) { return st * 128 + 64; }
+constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DK = 384, COL_DV = 448;
+__device__ __forceinline__ uint32_t col_dq(uint32_t buf) { return 128 + buf * 128; }
 
 // The CTA's task sequence: walk units blockIdx.x, +gridDim.x, ...; each unit a
 // run of R consecutive rows (full units) or a strided set of tail rows.
@@ -151,6 +163,24 @@ __device__ __forceinline__ bool wait_bar_warp(Shared* sh, int idx, uint32_t pari
   return ok != 0;
 }
 
+// 32 consecutive TMEM columns of this warp's lane quarter into registers.
+__device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&v)[32]) {
+  tmem_ld16(addr, *reinterpret_cast<uint32_t(*)[16]>(v));
+  tmem_ld16(addr + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+  tmem_ld_wait();
+}
+
+// 32 keys of row m (16 packed bf16 pairs) into the 128B-swizzled
+// [128 rows][64 keys] bf16 tile at base; half selects keys 0-31 or 32-63.
+__device__ __forceinline__ void store_row32(uint8_t* base, int m, int half, const uint32_t (&pk)[16]) {
+  uint8_t* row = base + m * 128;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t o = static_cast<uint32_t>(((half * 4 + c) ^ (m & 7)) << 4);
+    *reinterpret_cast<uint4*>(row + o) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+  }
+}
+
 }  // namespace ws
 
 __global__ void __launch_bounds__(ws::kThreads, 1)
@@ -165,8 +195,15 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    const uint32_t counts[INFO_FULL] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, kNumComp, kNumComp, kNumComp, 1,
-                                        1, kNumRed, 1, kNumRed, 2, 1, 1, 1, 1};
+    // TMA-filled and MMA-committed barriers take one arrival; the softmax
+    // warps' hand-offs (S/dP drained, P/dS stored) take one per softmax warp;
+    // the reduce warps' (dQ, dK/dV drained) one per reduce warp; DRAIN one
+    // per issuer.
+    uint32_t counts[INFO_FULL];
+    for (int i = 0; i < INFO_FULL; ++i) counts[i] = 1;
+    counts[S_EMPTY] = counts[PDS_FULL] = kNumComp;
+    counts[DQ_EMPTY] = counts[DQ_EMPTY + 1] = counts[DKV_EMPTY] = kNumRed;
+    counts[DRAIN] = 2;
     for (int i = 0; i < INFO_FULL; ++i) mbar_init(&sh->bar[i], counts[i]);
     for (int i = 0; i < kInfo; ++i) {
       mbar_init(&sh->bar[INFO_FULL + i], 1);
@@ -240,13 +277,13 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           const int hi = e.hi;
           if (hi < 0) break;
           if (e.flags & 1) {
-            const uint32_t seg = e.seg, kst = seg & 1;
-            if (!wait_bar(sh, K_EMPTY + kst, ((seg >> 1) & 1) ^ 1, a.status)) break;
+            const uint32_t seg = e.seg;
+            if (!wait_bar(sh, K_EMPTY, (seg & 1) ^ 1, a.status)) break;
             if (!wait_bar(sh, V_EMPTY, (seg & 1) ^ 1, a.status)) break;
-            uint64_t* fb = &sh->bar[KV_FULL + kst];
+            uint64_t* fb = &sh->bar[KV_FULL];
             mbar_arrive_expect_tx(fb, 32768u);
-            tma_load_3d(sm + OFF_K + kst * 16384, &tmK, fb, 0, hi, e.kvrow);
-            tma_load_3d(sm + OFF_K + kst * 16384 + 8192, &tmK, fb, 64, hi, e.kvrow);
+            tma_load_3d(sm + OFF_K, &tmK, fb, 0, hi, e.kvrow);
+            tma_load_3d(sm + OFF_K + 8192, &tmK, fb, 64, hi, e.kvrow);
             tma_load_3d(sm + OFF_V, &tmV, fb, 0, hi, e.kvrow);
             tma_load_3d(sm + OFF_V + 8192, &tmV, fb, 64, hi, e.kvrow);
           }
@@ -275,76 +312,82 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       }
     } else if (warp == kMmaWarp || warp == kMmaBWarp) {
       // ------------------------------------------------------------ MMA issuers
-      if (lane == 0) {
-        constexpr uint32_t ID_S = idesc_bf16_f32(128, 64, false, false);
-        constexpr uint32_t ID_T = idesc_bf16_f32(128, 64, true, true);
-        constexpr uint32_t ID_Q = idesc_bf16_f32(128, 128, false, true);
-        const uint32_t sb = smem_u32(sm);
-        // Descriptor bases; a K step or a stage is an immediate added to the
-        // 14-bit start-address field (byte offset >> 4; all addresses < 256 KB).
-        constexpr uint64_t kStageQ = QDO_STAGE >> 4, kStageK = 16384 >> 4;
-        const bool is_a = warp == kMmaWarp;
-        for (uint32_t j = 0;; ++j) {
-          const uint32_t slot = j % kInfo;
-          if (!wait_bar(sh, INFO_FULL + slot, (j / kInfo) & 1, a.status)) break;
-          const TaskInfo& e = sh->info[slot];
-          if (e.hi < 0) break;
-          const bool first = e.flags & 1, last = (e.flags >> 1) & 1;
-          const uint32_t seg = e.seg, kst = seg & 1;
-          const uint32_t st = j & 1, ph = (j >> 1) & 1;
-          if (is_a) {
-            // S = Q K^T, dP = dO V^T.  All dependencies are polled first and the 16
-            // MMAs then go out as one burst: any shared-memory access by the issuing
-            // thread between MMAs stalls the tensor core while it drains.
-            if (first && !wait_bar(sh, KV_FULL + kst, (seg >> 1) & 1, a.status)) break;
-            if (!wait_bar(sh, S_EMPTY + st, ph ^ 1, a.status)) break;
-            if (!wait_bar(sh, Q_FULL + st, ph, a.status)) break;
-            if (!wait_bar(sh, DO_FULL + st, ph, a.status)) break;
-            tc_fence_after();
-            const uint64_t qk = sdesc_sw128(sb + OFF_QDO, 16, 1024) + st * kStageQ;
-            const uint64_t kk0 = sdesc_sw128(sb + OFF_K, 16, 1024) + kst * kStageK;
-            const uint64_t dok = sdesc_sw128(sb + OFF_QDO + DO_IN_STAGE, 16, 1024) + st * kStageQ;
-            const uint64_t vk = sdesc_sw128(sb + OFF_V, 16, 1024);
+      // The whole warp runs the loop, so waits, task info and descriptors are
+      // warp-uniform; one elected lane issues each burst of MMAs and its
+      // commits.  (Issuing from a lone lane costs about 1.6x more per MMA.)
+      constexpr uint32_t ID_S = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t ID_T = idesc_bf16_f32(128, 64, true, true);
+      constexpr uint32_t ID_Q = idesc_bf16_f32(128, 128, false, true);
+      const uint32_t sb = smem_u32(sm);
+      // Descriptor bases; a K step or a stage is an immediate added to the
+      // 14-bit start-address field (byte offset >> 4; all addresses < 256 KB).
+      constexpr uint64_t kStageQ = QDO_STAGE >> 4;
+      const bool is_a = warp == kMmaWarp;
+      for (uint32_t j = 0;; ++j) {
+        const uint32_t slot = j % kInfo;
+        if (!wait_bar_warp(sh, INFO_FULL + slot, (j / kInfo) & 1, a.status)) break;
+        const TaskInfo& e = sh->info[slot];
+        const int hi = e.hi, flags = e.flags;
+        const uint32_t seg = e.seg;
+        __syncwarp();
+        if (hi < 0) break;
+        const bool first = flags & 1, last = (flags >> 1) & 1;
+        const uint32_t st = j & 1, ph = (j >> 1) & 1;  // Q/dO stage and dQ buffer
+        if (is_a) {
+          // S = Q K^T and dP = dO V^T, interleaved K step by K step
+          if (first && !wait_bar_warp(sh, KV_FULL, seg & 1, a.status)) break;
+          if (!wait_bar_warp(sh, S_EMPTY, (j & 1) ^ 1, a.status)) break;
+          if (!wait_bar_warp(sh, Q_FULL + st, ph, a.status)) break;
+          if (!wait_bar_warp(sh, DO_FULL + st, ph, a.status)) break;
+          tc_fence_after();
+          const uint64_t qk = sdesc_sw128(sb + OFF_QDO, 16, 1024) + st * kStageQ;
+          const uint64_t kk0 = sdesc_sw128(sb + OFF_K, 16, 1024);
+          const uint64_t dok = sdesc_sw128(sb + OFF_QDO + DO_IN_STAGE, 16, 1024) + st * kStageQ;
+          const uint64_t vk = sdesc_sw128(sb + OFF_V, 16, 1024);
+          if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_bf16(tmem + col_s(st), qk + (kk >> 2) * 1024 + (kk & 3) * 2, kk0 + (kk >> 2) * 512 + (kk & 3) * 2,
-                        ID_S, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_bf16(tmem + col_dp(st), dok + (kk >> 2) * 1024 + (kk & 3) * 2, vk + (kk >> 2) * 512 + (kk & 3) * 2,
-                        ID_S, kk > 0);
-            umma_commit(&sh->bar[S_FULL + st]);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ao = (kk >> 2) * 1024 + (kk & 3) * 2, bo = (kk >> 2) * 512 + (kk & 3) * 2;
+              umma_bf16(tmem + COL_S, qk + ao, kk0 + bo, ID_S, kk > 0);
+              umma_bf16(tmem + COL_DP, dok + ao, vk + bo, ID_S, kk > 0);
+            }
+            umma_commit(&sh->bar[S_FULL]);
             if (last) umma_commit(&sh->bar[V_EMPTY]);
-          } else {
-            // dK^T += Q^T dS, dV^T += dO^T P, dQ = dS K, as one burst of 20 MMAs
-            if (!wait_bar(sh, PDS_FULL, j & 1, a.status)) break;
-            if (first && !wait_bar(sh, DKV_EMPTY, (seg & 1) ^ 1, a.status)) break;
-            if (!wait_bar(sh, DQ_EMPTY, (j & 1) ^ 1, a.status)) break;
-            tc_fence_after();
-            const uint32_t acc0 = first ? 0u : 1u;
-            const uint64_t qm = sdesc_sw128(sb + OFF_QDO, 16384, 1024) + st * kStageQ;
-            const uint64_t dsm = sdesc_sw128(sb + OFF_DS, 8192, 1024);
-            const uint64_t dom = sdesc_sw128(sb + OFF_QDO + DO_IN_STAGE, 16384, 1024) + st * kStageQ;
-            const uint64_t pm = sdesc_sw128(sb + OFF_P, 8192, 1024);
-            const uint64_t dsk = sdesc_sw128(sb + OFF_DS, 16, 1024);
-            const uint64_t km = sdesc_sw128(sb + OFF_K, 8192, 1024) + kst * kStageK;
+          }
+          __syncwarp();
+        } else {
+          // dV^T += dO^T P, dK^T += Q^T dS and dQ = dS K, interleaved.  P/dS
+          // are stored after S/dP completed, so every MMA of the task that
+          // reads this Q/dO stage has completed by the commits below.
+          if (!wait_bar_warp(sh, PDS_FULL, j & 1, a.status)) break;
+          if (first && !wait_bar_warp(sh, DKV_EMPTY, (seg & 1) ^ 1, a.status)) break;
+          if (!wait_bar_warp(sh, DQ_EMPTY + st, ph ^ 1, a.status)) break;
+          tc_fence_after();
+          const uint32_t acc0 = first ? 0u : 1u;
+          const uint64_t dom = sdesc_sw128(sb + OFF_QDO + DO_IN_STAGE, 16384, 1024) + st * kStageQ;
+          const uint64_t pm = sdesc_sw128(sb + OFF_P, 8192, 1024);
+          const uint64_t qm = sdesc_sw128(sb + OFF_QDO, 16384, 1024) + st * kStageQ;
+          const uint64_t dsm = sdesc_sw128(sb + OFF_DS, 8192, 1024);
+          const uint64_t dsk = sdesc_sw128(sb + OFF_DS, 16, 1024);
+          const uint64_t km = sdesc_sw128(sb + OFF_K, 8192, 1024);
+          const uint32_t dq = tmem + col_dq(st);
+          if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_bf16(tmem + COL_DK, qm + kk * 128, dsm + kk * 128, ID_T, kk > 0 ? 1u : acc0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
+            for (int kk = 0; kk < 8; ++kk) {
               umma_bf16(tmem + COL_DV, dom + kk * 128, pm + kk * 128, ID_T, kk > 0 ? 1u : acc0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + COL_DQ, dsk + kk * 2, km + kk * 128, ID_Q, kk > 0);
+              umma_bf16(tmem + COL_DK, qm + kk * 128, dsm + kk * 128, ID_T, kk > 0 ? 1u : acc0);
+              if (kk & 1) umma_bf16(dq, dsk + (kk >> 1) * 2, km + (kk >> 1) * 128, ID_Q, kk > 1);
+            }
+            umma_commit(&sh->bar[PDS_EMPTY]);
             umma_commit(&sh->bar[Q_EMPTY + st]);
             umma_commit(&sh->bar[DO_EMPTY + st]);
-            umma_commit(&sh->bar[PDS_EMPTY]);
-            umma_commit(&sh->bar[DQ_FULL]);
+            umma_commit(&sh->bar[DQ_FULL + st]);
             if (last) {
-              umma_commit(&sh->bar[K_EMPTY + kst]);
+              umma_commit(&sh->bar[K_EMPTY]);
               umma_commit(&sh->bar[DKV_FULL]);
             }
           }
+          __syncwarp();
         }
       }
     } else if (warp < kRed0) {
@@ -378,19 +421,21 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           const bool nmore = ne.hi >= 0;
           const int nb = ne.b;
           if (nmore) fetch(ne, nqpos, nlse2, ndsc);
-          const uint32_t qst = j & 1;
-          if (!wait_bar_warp(sh, S_FULL + qst, (j >> 1) & 1, a.status)) break;
+          const uint32_t par = j & 1;
+          const int kbase = b * 64 + half * 32;
+          if (!wait_bar_warp(sh, S_FULL, par, a.status)) break;
           tc_fence_after();
           uint32_t sv[32], dpv[32];
-          tmem_ld16(tmem + lane_base + col_s(qst) + half * 32, *reinterpret_cast<uint32_t(*)[16]>(sv));
-          tmem_ld16(tmem + lane_base + col_s(qst) + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(sv + 16));
-          tmem_ld16(tmem + lane_base + col_dp(qst) + half * 32, *reinterpret_cast<uint32_t(*)[16]>(dpv));
-          tmem_ld16(tmem + lane_base + col_dp(qst) + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(dpv + 16));
+          tmem_ld16(tmem + lane_base + COL_S + half * 32, *reinterpret_cast<uint32_t(*)[16]>(sv));
+          tmem_ld16(tmem + lane_base + COL_S + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(sv + 16));
+          tmem_ld16(tmem + lane_base + COL_DP + half * 32, *reinterpret_cast<uint32_t(*)[16]>(dpv));
+          tmem_ld16(tmem + lane_base + COL_DP + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(dpv + 16));
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sh->bar[S_EMPTY + qst]);
-          const int kbase = b * 64 + half * 32;
+          if (lane == 0) mbar_arrive(&sh->bar[S_EMPTY]);
+          // P = exp2(S * scale * log2e - LSE * log2e) on the causal mask and
+          // dS = P * (dP * scale - D * scale); masked entries are exactly 0
           uint32_t pk[16], dk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
@@ -405,15 +450,9 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
             pk[e >> 1] = pack_bf16x2(p[0], p[1]);
             dk[e >> 1] = pack_bf16x2(ds[0], ds[1]);
           }
-          if (!wait_bar_warp(sh, PDS_EMPTY, (j & 1) ^ 1, a.status)) break;
-          uint8_t* prow = sm + OFF_P + m * 128;
-          uint8_t* drow = sm + OFF_DS + m * 128;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t o = static_cast<uint32_t>(((half * 4 + c) ^ (m & 7)) << 4);
-            *reinterpret_cast<uint4*>(prow + o) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            *reinterpret_cast<uint4*>(drow + o) = make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
-          }
+          if (!wait_bar_warp(sh, PDS_EMPTY, par ^ 1, a.status)) break;
+          store_row32(sm + OFF_P, m, half, pk);
+          store_row32(sm + OFF_DS, m, half, dk);
           fence_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh->bar[PDS_FULL]);
@@ -423,9 +462,14 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
     comp_done:;
     } else {
       // ------------------------------------------------------------ reduce
+      // Warp sp owns TMEM lanes 32*sp..: dQ rows of tokens 2*sp, 2*sp+1 and
+      // head-dim rows 32*sp.. of dK^T/dV^T.  Each 4 KB chunk goes through one
+      // of the warp's two staging slots as its own bulk group, so refilling a
+      // slot only waits for the reduce-add issued two chunks earlier.
       const int sp = warp & 3;
       const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
-      uint8_t* stg = sm + OFF_ST + (warp - kRed0) * 4096;
+      uint8_t* stg0 = sm + OFF_ST + (warp - kRed0) * 8192;
+      uint32_t chunk = 0;
       for (uint32_t j = 0;; ++j) {
         const uint32_t slot = j % kInfo;
         if (!wait_bar_warp(sh, INFO_FULL + slot, (j / kInfo) & 1, a.status)) break;
@@ -434,24 +478,27 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         const uint32_t seg = e.seg;
         __syncwarp();
         if (hi < 0) break;
-        if (!wait_bar_warp(sh, DQ_FULL, j & 1, a.status)) break;
+        const uint32_t pb = j & 1;
+        if (!wait_bar_warp(sh, DQ_FULL + pb, (j >> 1) & 1, a.status)) break;
         tc_fence_after();
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t v[64];
-          tmem_ld16(tmem + lane_base + COL_DQ + hf * 64, *reinterpret_cast<uint32_t(*)[16]>(v));
-          tmem_ld16(tmem + lane_base + COL_DQ + hf * 64 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-          tmem_ld16(tmem + lane_base + COL_DQ + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[16]>(v + 32));
-          tmem_ld16(tmem + lane_base + COL_DQ + hf * 64 + 48, *reinterpret_cast<uint32_t(*)[16]>(v + 48));
+          const uint32_t col = col_dq(pb) + hf * 64;
+          tmem_ld16(tmem + lane_base + col, *reinterpret_cast<uint32_t(*)[16]>(v));
+          tmem_ld16(tmem + lane_base + col + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+          tmem_ld16(tmem + lane_base + col + 32, *reinterpret_cast<uint32_t(*)[16]>(v + 32));
+          tmem_ld16(tmem + lane_base + col + 48, *reinterpret_cast<uint32_t(*)[16]>(v + 48));
           tmem_ld_wait();
           if (hf == 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sh->bar[DQ_EMPTY]);
+            if (lane == 0) mbar_arrive(&sh->bar[DQ_EMPTY + pb]);
           }
 #pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            if (lane == 0) bulk_wait_read_all();
+          for (int q2 = 0; q2 < 2; ++q2, ++chunk) {
+            uint8_t* stg = stg0 + (chunk & 1) * 4096;
+            if (lane == 0) bulk_wait_read_but_one();
             __syncwarp();
 #pragma unroll
             for (int c = 0; c < 8; ++c)
@@ -469,19 +516,18 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           if (!wait_bar_warp(sh, DKV_FULL, seg & 1, a.status)) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < 4; ++q, ++chunk) {
             const int which = q >> 1, kh = q & 1;
             uint32_t v[32];
             const uint32_t col = (which ? COL_DV : COL_DK) + kh * 32;
-            tmem_ld16(tmem + lane_base + col, *reinterpret_cast<uint32_t(*)[16]>(v));
-            tmem_ld16(tmem + lane_base + col + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-            tmem_ld_wait();
+            tmem_ld32(tmem + lane_base + col, v);
             if (q == 3) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&sh->bar[DKV_EMPTY]);
             }
-            if (lane == 0) bulk_wait_read_all();
+            uint8_t* stg = stg0 + (chunk & 1) * 4096;
+            if (lane == 0) bulk_wait_read_but_one();
             __syncwarp();
 #pragma unroll
             for (int ee = 0; ee < 32; ++ee)
@@ -502,10 +548,14 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
     }
   }
   __syncwarp();
-  // drain: make sure no MMA is still writing TMEM before it is released
-  if ((warp == kMmaWarp || warp == kMmaBWarp) && lane == 0) {
-    umma_commit(&sh->bar[DRAIN]);
-    wait_bar(sh, DRAIN, 0, a.status, false);
+  // drain: make sure no MMA is still writing TMEM before it is released (the
+  // elected lane is the one that issued, the lowest lane of the warp)
+  if (warp == kMmaWarp || warp == kMmaBWarp) {
+    if (elect_one()) {
+      umma_commit(&sh->bar[DRAIN]);
+      wait_bar(sh, DRAIN, 0, a.status, false);
+    }
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();

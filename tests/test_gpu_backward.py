@@ -140,11 +140,27 @@ def test_aligned_workspace_padding_rows_are_zero(B):
     assert not dk[pad].any() and not dv[pad].any()
 
 
-def test_backward_is_repeatable_within_tolerance(B):
-    pb = W.make_problem("tiny")
-    o_bits, lse32 = oracle_forward_stored(pb)
-    a = _run_gpu(B, pb, o_bits, lse32)
-    b = _run_gpu(B, pb, o_bits, lse32)
-    for x, y in zip(a, b):
-        d = np.abs(O.bf16_to_f64(x) - O.bf16_to_f64(y))
-        assert d.max() <= 2 * O.bf16_ulp(np.maximum(np.abs(O.bf16_to_f64(x)), 1e-3)).max()
+@pytest.mark.parametrize("name,tile", [("tiny", 0), ("single8k", 0), ("single8k", 16)])
+def test_backward_is_repeatable_within_tolerance(B, name, tile):
+    """Three runs on the same inputs agree to within two bf16 ulps: only the
+    order of the fp32 reduce-adds may differ between runs, so a pipeline race
+    (an operand consumed before it lands, a buffer overwritten while read)
+    shows up here even when it happens to stay inside the oracle tolerance."""
+    import torch
+    pb = W.make_problem(name)
+    prob, t = upload(pb)
+    o, lse, st = B.forward(prob, t["sel"], t["q"], t["k"], t["v"])
+    torch.cuda.synchronize()
+    assert int(st[0].item()) == 0
+    runs = []
+    for _ in range(3):
+        bw = B.Backward(prob, task_tile_chunks=tile)
+        outs = bw.run(t["sel"], t["q"], t["k"], t["v"], o, t["do"], lse)
+        torch.cuda.synchronize()
+        bw.check_status()
+        runs.append([O.bf16_to_f64(from_bf16_tensor(x)) for x in outs])
+    for other in runs[1:]:
+        for x, y in zip(runs[0], other):
+            assert np.all(np.isfinite(y))
+            tol = 2 * O.bf16_ulp(np.maximum(np.abs(x), 1e-3))
+            assert np.all(np.abs(x - y) <= tol)
