@@ -78,11 +78,16 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DK = 384, COL_DV = 448;
 __device__ __forceinline__ uint32_t col_dq(uint32_t buf) { return 128 + buf * 128; }
 
-// The CTA's task sequence: walk units blockIdx.x, +gridDim.x, ...; each unit a
-// run of R consecutive rows (full units) or a strided set of tail rows.
+// The CTA's task sequence.  The walk's units are the pages' (full units of R
+// consecutive rows, then tail units of rows strided by the tail-unit count),
+// but a CTA takes its next unit from a global counter when it has finished the
+// last one, instead of the static unit blockIdx.x + k * gridDim.x: the CTAs
+// then stay within a few units of one another in the row order, which keeps
+// the query tiles they touch at the same time small enough to stay in L2.
 struct Walk {
   int n, R, full, grid;
   int u, i, cnt, t0, step;
+  int32_t* ctr;
   __device__ __forceinline__ void setup() {
     if (u >= grid) return;
     if (u < full) {
@@ -91,16 +96,17 @@ struct Walk {
       step = grid - full; t0 = full * R + (u - full); cnt = (n - t0 + step - 1) / step;
     }
   }
-  __device__ __forceinline__ void init(const int32_t* walk) {
+  __device__ __forceinline__ void init(const int32_t* walk, int32_t* unit_ctr) {
     n = walk[MSA_WALK_ROWS]; R = walk[MSA_WALK_ROWS_PER_CTA];
     full = walk[MSA_WALK_FULL]; grid = walk[MSA_WALK_GRID];
-    u = blockIdx.x; i = 0;
+    ctr = unit_ctr;
+    u = atomicAdd(ctr, 1); i = 0;
     setup();
   }
   __device__ __forceinline__ int take() {  // current task or -1, then advance
     if (u >= grid) return -1;
     const int t = t0 + i * step;
-    if (++i >= cnt) { u += gridDim.x; i = 0; setup(); }
+    if (++i >= cnt) { u = atomicAdd(ctr, 1); i = 0; setup(); }
     return t;
   }
 };
@@ -109,8 +115,8 @@ struct Walk {
 struct Seq {
   Walk w;
   int cur, nxt;
-  __device__ __forceinline__ void init(const int32_t* walk) {
-    w.init(walk);
+  __device__ __forceinline__ void init(const int32_t* walk, int32_t* unit_ctr) {
+    w.init(walk, unit_ctr);
     cur = w.take();
     nxt = w.take();
   }
@@ -227,7 +233,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       // ------------------------------------------------------------ task info
       if (lane == 0) {
         Seq s;
-        s.init(a.walk);
+        s.init(a.walk, a.unit_ctr);
         uint32_t j = 0, nseg = 0;
         int64_t prev = -1;
         int64_t key = s.cur >= 0 ? bucket_key(meta, s.cur) : -1;
@@ -270,6 +276,9 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         tma_prefetch_desc(&tmdO);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        // Q/dO tiles are reused by every task of their query chunk within the
+        // query tile; a K/V tile only within its bucket segment
+        const uint64_t keep = l2_evict_last(), stream = l2_evict_first();
         for (uint32_t j = 0;; ++j) {
           const uint32_t slot = j % kInfo;
           if (!wait_bar(sh, INFO_FULL + slot, (j / kInfo) & 1, a.status)) break;
@@ -282,30 +291,32 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
             if (!wait_bar(sh, V_EMPTY, (seg & 1) ^ 1, a.status)) break;
             uint64_t* fb = &sh->bar[KV_FULL];
             mbar_arrive_expect_tx(fb, 32768u);
-            tma_load_3d(sm + OFF_K, &tmK, fb, 0, hi, e.kvrow);
-            tma_load_3d(sm + OFF_K + 8192, &tmK, fb, 64, hi, e.kvrow);
-            tma_load_3d(sm + OFF_V, &tmV, fb, 0, hi, e.kvrow);
-            tma_load_3d(sm + OFF_V + 8192, &tmV, fb, 64, hi, e.kvrow);
+            tma_load_3d_hint(sm + OFF_K, &tmK, fb, 0, hi, e.kvrow, stream);
+            tma_load_3d_hint(sm + OFF_K + 8192, &tmK, fb, 64, hi, e.kvrow, stream);
+            tma_load_3d_hint(sm + OFF_V, &tmV, fb, 0, hi, e.kvrow, stream);
+            tma_load_3d_hint(sm + OFF_V + 8192, &tmV, fb, 64, hi, e.kvrow, stream);
           }
           const uint32_t qst = j & 1, qph = ((j >> 1) & 1) ^ 1;
           uint8_t* st = sm + OFF_QDO + qst * QDO_STAGE;
           if (!wait_bar(sh, Q_EMPTY + qst, qph, a.status)) break;
           mbar_arrive_expect_tx(&sh->bar[Q_FULL + qst], 32768u);
-          tma_load_3d(st, &tmQ, &sh->bar[Q_FULL + qst], 0, hi * 16, e.tok0);
-          tma_load_3d(st + 16384, &tmQ, &sh->bar[Q_FULL + qst], 64, hi * 16, e.tok0);
+          const int qrow = hi * a.T + e.tok0;  // Q and dO are index-head-major
+          tma_load_3d_hint(st, &tmQ, &sh->bar[Q_FULL + qst], 0, 0, qrow, keep);
+          tma_load_3d_hint(st + 16384, &tmQ, &sh->bar[Q_FULL + qst], 64, 0, qrow, keep);
           if (!wait_bar(sh, DO_EMPTY + qst, qph, a.status)) break;
           mbar_arrive_expect_tx(&sh->bar[DO_FULL + qst], 32768u);
-          tma_load_3d(st + DO_IN_STAGE, &tmdO, &sh->bar[DO_FULL + qst], 0, hi * 16, e.tok0);
-          tma_load_3d(st + DO_IN_STAGE + 16384, &tmdO, &sh->bar[DO_FULL + qst], 64, hi * 16, e.tok0);
+          tma_load_3d_hint(st + DO_IN_STAGE, &tmdO, &sh->bar[DO_FULL + qst], 0, 0, qrow, keep);
+          tma_load_3d_hint(st + DO_IN_STAGE + 16384, &tmdO, &sh->bar[DO_FULL + qst], 64, 0, qrow, keep);
           // warm L2 with the query tiles of the task two ahead, if its info is published
           const uint32_t ps = (j + 2) % kInfo;
           if (mbar_test_wait(&sh->bar[INFO_FULL + ps], ((j + 2) / kInfo) & 1)) {
             const TaskInfo& f = sh->info[ps];
             if (f.hi >= 0) {
-              tma_prefetch_l2_3d(&tmQ, 0, f.hi * 16, f.tok0);
-              tma_prefetch_l2_3d(&tmQ, 64, f.hi * 16, f.tok0);
-              tma_prefetch_l2_3d(&tmdO, 0, f.hi * 16, f.tok0);
-              tma_prefetch_l2_3d(&tmdO, 64, f.hi * 16, f.tok0);
+              const int frow = f.hi * a.T + f.tok0;
+              tma_prefetch_l2_3d_hint(&tmQ, 0, 0, frow, keep);
+              tma_prefetch_l2_3d_hint(&tmQ, 64, 0, frow, keep);
+              tma_prefetch_l2_3d_hint(&tmdO, 0, 0, frow, keep);
+              tma_prefetch_l2_3d_hint(&tmdO, 64, 0, frow, keep);
             }
           }
         }
@@ -470,6 +481,9 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
       uint8_t* stg0 = sm + OFF_ST + (warp - kRed0) * 8192;
       uint32_t chunk = 0;
+      // the dQ accumulator rows of a query chunk take a reduce-add from every
+      // task of the chunk; a dK/dV tile one per bucket segment
+      const uint64_t keep = l2_evict_last(), stream = l2_evict_first();
       for (uint32_t j = 0;; ++j) {
         const uint32_t slot = j % kInfo;
         if (!wait_bar_warp(sh, INFO_FULL + slot, (j / kInfo) & 1, a.status)) break;
@@ -507,7 +521,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_reduce_add_3d(&tmdQ, stg, hf * 64 + q2 * 32, hi * 16, tok0 + 2 * sp);
+              tma_reduce_add_3d_hint(&tmdQ, stg, hf * 64 + q2 * 32, 0, hi * a.T + tok0 + 2 * sp, keep);
               bulk_commit();
             }
           }
@@ -535,7 +549,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_reduce_add_3d(which ? &tmdV : &tmdK, stg, sp * 32, hi, kvrow + kh * 32);
+              tma_reduce_add_3d_hint(which ? &tmdV : &tmdK, stg, sp * 32, 0, hi * a.W + kvrow + kh * 32, stream);
               bulk_commit();
             }
           }

@@ -63,6 +63,8 @@ size_t bwd_ws_bytes(const msa_problem* p) {
   size_t b = round_up(sizeof(float) * T * Hq, 256);                 // D
   b += round_up(sizeof(float) * T * Hq * kHeadDim, 256);            // dQ accumulator
   b += 2 * round_up(sizeof(float) * W * Hkv * kHeadDim, 256);       // dK, dV accumulators
+  b += 2 * round_up(sizeof(uint16_t) * T * Hq * kHeadDim, 256);     // index-head-major Q, dO
+  b += 256;                                                          // walk-unit counter
   return b;
 }
 
