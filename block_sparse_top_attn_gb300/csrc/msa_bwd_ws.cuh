@@ -406,24 +406,22 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       const int sp = warp & 3, half = (warp - kComp0) >> 2;
       const int m = sp * 32 + lane, slot_row = m >> 4, hh = m & 15;
       const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
-      // per-row LSE and D of the next task, loaded one task ahead
-      auto fetch = [&](const TaskInfo& e, int& qpos, float& lse2, float& dsc) {
+      // Per-row LSE and D of the next task, loaded one task ahead.  The raw
+      // values are only consumed in the next iteration, so the loads stay in
+      // flight across this task instead of stalling the warp here.
+      auto fetch = [&](const TaskInfo& e, int& qpos, float& lse_raw, float& dlt_raw) {
         qpos = e.qpos[slot_row];
-        lse2 = 0.f;
-        dsc = 0.f;
-        if (qpos >= 0) {
-          const int64_t row = (int64_t)(e.tok0 + slot_row) * a.Hq + e.hi * 16 + hh;
-          lse2 = a.lse[row] * kLog2e;
-          dsc = a.delta[row] * a.scale;
-        }
+        const int64_t row = (int64_t)(e.tok0 + slot_row) * a.Hq + e.hi * 16 + hh;
+        lse_raw = qpos >= 0 ? a.lse[row] : 0.f;
+        dlt_raw = qpos >= 0 ? a.delta[row] : 0.f;
       };
       if (!wait_bar_warp(sh, INFO_FULL + 0, 0, a.status)) goto comp_done;
       {
         int qpos, nqpos = -1;
-        float lse2, dsc, nlse2 = 0.f, ndsc = 0.f;
+        float lse_raw, dlt_raw, nlse_raw = 0.f, ndlt_raw = 0.f;
         int b = sh->info[0].b;
         bool more = sh->info[0].hi >= 0;
-        if (more) fetch(sh->info[0], qpos, lse2, dsc);
+        if (more) fetch(sh->info[0], qpos, lse_raw, dlt_raw);
         for (uint32_t j = 0; more; ++j) {
           // look ahead: next task's info and its per-row scalars
           const uint32_t nslot = (j + 1) % kInfo;
@@ -431,35 +429,47 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           const TaskInfo& ne = sh->info[nslot];
           const bool nmore = ne.hi >= 0;
           const int nb = ne.b;
-          if (nmore) fetch(ne, nqpos, nlse2, ndsc);
+          if (nmore) fetch(ne, nqpos, nlse_raw, ndlt_raw);
           const uint32_t par = j & 1;
           const int kbase = b * 64 + half * 32;
           if (!wait_bar_warp(sh, S_FULL, par, a.status)) break;
           tc_fence_after();
           uint32_t sv[32], dpv[32];
-          tmem_ld16(tmem + lane_base + COL_S + half * 32, *reinterpret_cast<uint32_t(*)[16]>(sv));
-          tmem_ld16(tmem + lane_base + COL_S + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(sv + 16));
-          tmem_ld16(tmem + lane_base + COL_DP + half * 32, *reinterpret_cast<uint32_t(*)[16]>(dpv));
-          tmem_ld16(tmem + lane_base + COL_DP + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(dpv + 16));
+          tmem_ld32x(tmem + lane_base + COL_S + half * 32, sv);
+          tmem_ld32x(tmem + lane_base + COL_DP + half * 32, dpv);
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh->bar[S_EMPTY]);
+          const float lse2 = lse_raw * kLog2e, dsc = dlt_raw * a.scale;
           // P = exp2(S * scale * log2e - LSE * log2e) on the causal mask and
           // dS = P * (dP * scale - D * scale); masked entries are exactly 0
           uint32_t pk[16], dk[16];
+          const int lim = qpos - kbase;  // keys kbase + e with e <= lim are attended
+          if (lim >= 31) {
+            // the whole 32-key slice is attended (every block but the diagonal one)
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float p[2], ds[2];
-#pragma unroll
-            for (int x = 0; x < 2; ++x) {
-              const bool valid = kbase + e + x <= qpos;
-              const float pv = ex2_approx(fmaf(__uint_as_float(sv[e + x]), a.scale_log2, -lse2));
-              p[x] = valid ? pv : 0.f;
-              ds[x] = valid ? pv * fmaf(__uint_as_float(dpv[e + x]), a.scale, -dsc) : 0.f;
+            for (int e = 0; e < 32; e += 2) {
+              const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), a.scale_log2, -lse2));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), a.scale_log2, -lse2));
+              pk[e >> 1] = pack_bf16x2(p0, p1);
+              dk[e >> 1] = pack_bf16x2(p0 * fmaf(__uint_as_float(dpv[e]), a.scale, -dsc),
+                                       p1 * fmaf(__uint_as_float(dpv[e + 1]), a.scale, -dsc));
             }
-            pk[e >> 1] = pack_bf16x2(p[0], p[1]);
-            dk[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float p[2], ds[2];
+#pragma unroll
+              for (int x = 0; x < 2; ++x) {
+                const bool valid = e + x <= lim;
+                const float pv = ex2_approx(fmaf(__uint_as_float(sv[e + x]), a.scale_log2, -lse2));
+                p[x] = valid ? pv : 0.f;
+                ds[x] = valid ? pv * fmaf(__uint_as_float(dpv[e + x]), a.scale, -dsc) : 0.f;
+              }
+              pk[e >> 1] = pack_bf16x2(p[0], p[1]);
+              dk[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+            }
           }
           if (!wait_bar_warp(sh, PDS_EMPTY, par ^ 1, a.status)) break;
           store_row32(sm + OFF_P, m, half, pk);
@@ -467,7 +477,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           fence_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh->bar[PDS_FULL]);
-          qpos = nqpos; lse2 = nlse2; dsc = ndsc; b = nb; more = nmore;
+          qpos = nqpos; lse_raw = nlse_raw; dlt_raw = ndlt_raw; b = nb; more = nmore;
         }
       }
     comp_done:;
