@@ -277,7 +277,8 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         // Q/dO tiles are reused by every task of their query chunk within the
-        // query tile; a K/V tile only within its bucket segment
+        // query tile (they stay in L2 while the CTAs walk the tile together);
+        // a K/V tile only within its bucket segment
         const uint64_t keep = l2_evict_last(), stream = l2_evict_first();
         for (uint32_t j = 0;; ++j) {
           const uint32_t slot = j % kInfo;
@@ -307,18 +308,6 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           mbar_arrive_expect_tx(&sh->bar[DO_FULL + qst], 32768u);
           tma_load_3d_hint(st + DO_IN_STAGE, &tmdO, &sh->bar[DO_FULL + qst], 0, 0, qrow, keep);
           tma_load_3d_hint(st + DO_IN_STAGE + 16384, &tmdO, &sh->bar[DO_FULL + qst], 64, 0, qrow, keep);
-          // warm L2 with the query tiles of the task two ahead, if its info is published
-          const uint32_t ps = (j + 2) % kInfo;
-          if (mbar_test_wait(&sh->bar[INFO_FULL + ps], ((j + 2) / kInfo) & 1)) {
-            const TaskInfo& f = sh->info[ps];
-            if (f.hi >= 0) {
-              const int frow = f.hi * a.T + f.tok0;
-              tma_prefetch_l2_3d_hint(&tmQ, 0, 0, frow, keep);
-              tma_prefetch_l2_3d_hint(&tmQ, 64, 0, frow, keep);
-              tma_prefetch_l2_3d_hint(&tmdO, 0, 0, frow, keep);
-              tma_prefetch_l2_3d_hint(&tmdO, 64, 0, frow, keep);
-            }
-          }
         }
       }
     } else if (warp == kMmaWarp || warp == kMmaBWarp) {
