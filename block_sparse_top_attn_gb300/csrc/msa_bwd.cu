@@ -2,7 +2,7 @@
 // tcgen05 kernel and postprocess ("msa_backward_sm100" page: KV-parallel task
 // rows of 8 queries x 16 heads bucketed by (batch, index head, key block); five
 // GEMMs S, dP, dV, dK, dQ; dK/dV accumulated per bucket segment; dQ reduced
-// into an accumulator that the postprocess casts to bf16).
+// in bf16 across tasks, as the pages' bf16 dQ pool is).
 //
 // Main kernel data flow for one task (128 rows = 8 tokens x 16 q-heads, one
 // key block of 64 keys, head_dim 128), all GEMMs M = 128 with fp32 in TMEM:
@@ -14,10 +14,11 @@
 //   dK^T [d, key] += Q^T  . dS          A = Q  (MN-major) B = dS (MN-major)
 //   dQ   [row, d]  = dS . K             A = dS (K-major)  B = K  (MN-major)
 // Q, dO, K, V arrive by TMA with 128-byte swizzle; P and dS are written in the
-// same swizzled layout, so no operand is ever transposed in memory.  dQ is
-// reduced into an fp32 accumulator with TMA bulk reduce-add per task; dK^T and
-// dV^T stay in TMEM for a bucket segment and are reduced the same way when the
-// segment ends.
+// same swizzled layout, so no operand is ever transposed in memory.  A task's
+// dQ (fp32 in TMEM over its 64 keys) is rounded to bf16 and reduced straight
+// into the bf16 dQ output with a TMA bulk reduce-add; dK^T and dV^T stay in
+// TMEM for a bucket segment and are reduced into fp32 accumulators when the
+// segment ends, which the postprocess casts to bf16.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -31,8 +32,8 @@ namespace msa {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
-// preprocess: D[t, h] = sum_d dO * O (fp32), zeroed fp32 accumulators, and
-// index-head-major copies of Q and dO for the main kernel.
+// preprocess: D[t, h] = sum_d dO * O (fp32), zeroed dK/dV fp32 accumulators and
+// bf16 dQ output, and index-head-major copies of Q and dO for the main kernel.
 //
 // Index-head-major ([Hi][T][16][128]) puts one task's 8 tokens x 16 q-heads in
 // one contiguous block.  In the [T][Hq][128] layout that block is 8 pieces at a
@@ -43,7 +44,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
                                                           const uint4* __restrict__ q, uint4* __restrict__ qh,
                                                           uint4* __restrict__ doh, float* __restrict__ delta,
                                                           int64_t T, int Hq, float4* __restrict__ zero,
-                                                          int64_t zero_n4, const int32_t* status) {
+                                                          int64_t zero_n4, uint4* __restrict__ dq,
+                                                          const int32_t* status) {
   if (status_bad(status)) return;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
@@ -71,6 +73,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
   }
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int64_t i = tid; i < zero_n4; i += nthr) zero[i] = z;
+  // dQ is reduced straight into the bf16 output
+  const uint4 zb = make_uint4(0, 0, 0, 0);
+  for (int64_t i = tid; i < total16; i += nthr) dq[i] = zb;
 }
 
 // ---------------------------------------------------------------------------
@@ -81,12 +86,10 @@ __device__ __forceinline__ uint4 cast8(const float4* src) {
   return make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
 }
 
-// The accumulators are index-head-major: dQ [Hi][T][16][128] (one task's 8
-// tokens x 16 heads are one contiguous 64 KB block) and dK, dV [Hkv][W][128];
-// the outputs are [T][Hq][128] and [W][Hkv][128].
-__global__ void __launch_bounds__(256) postprocess_kernel(const float4* __restrict__ dq_acc, uint4* __restrict__ dq,
-                                                           int64_t dq_n8, int64_t T, int Hq,
-                                                           const float4* __restrict__ dk_acc,
+// The dK, dV accumulators are index-head-major, [Hkv][W][128]; the outputs are
+// [W][Hkv][128].  (dQ needs no postprocess: it is reduced straight into its
+// bf16 output.)
+__global__ void __launch_bounds__(256) postprocess_kernel(const float4* __restrict__ dk_acc,
                                                            const float4* __restrict__ dv_acc, uint4* __restrict__ dk,
                                                            uint4* __restrict__ dv, int64_t kv_n8, int64_t W, int Hkv,
                                                            const int32_t* cu, const int32_t* kvs, int N,
@@ -94,14 +97,6 @@ __global__ void __launch_bounds__(256) postprocess_kernel(const float4* __restri
   if (status_bad(status)) return;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
-  const int hq16 = Hq * 16;  // 8-element groups per token row
-  for (int64_t i = tid; i < dq_n8; i += nthr) {
-    const int64_t t = i / hq16;
-    const int r = (int)(i - t * hq16);        // 8-element group within the token row
-    const int h = r >> 4, g = r & 15;         // q-head, group within the head
-    const int64_t src = ((int64_t)(h >> 4) * T + t) * 256 + (h & 15) * 16 + g;  // in units of 8 floats
-    dq[i] = cast8(dq_acc + 2 * src);
-  }
   const int kv_row_n8 = Hkv * 16;
   for (int64_t i = tid; i < kv_n8; i += nthr) {
     const int64_t row = i / kv_row_n8;
@@ -135,7 +130,7 @@ struct MainArgs {
   const int32_t* walk;
   const int32_t* kv_doc_starts;
   int Hq;
-  int T;              // rows of the token axis (Q, dO and the dQ accumulator are [Hi][T][16][128])
+  int T;              // rows of the token axis (the Q, dO copies are [Hi][T][16][128])
   int W;              // rows of the K/V axis (the dK, dV accumulators are [Hkv][W][128])
   int32_t* unit_ctr;  // next walk unit to hand out; 0 at launch
   float scale_log2;
@@ -170,13 +165,11 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* delta = reinterpret_cast<float*>(w);
   w += round_up(sizeof(float) * T * Hq, 256);
-  float* dq_acc = reinterpret_cast<float*>(w);
-  w += round_up(sizeof(float) * T * Hq * kHeadDim, 256);
   float* dk_acc = reinterpret_cast<float*>(w);
   w += round_up(sizeof(float) * W * Hkv * kHeadDim, 256);
   float* dv_acc = reinterpret_cast<float*>(w);
   w += round_up(sizeof(float) * W * Hkv * kHeadDim, 256);
-  const int64_t zero_n4 = (reinterpret_cast<float*>(w) - dq_acc) / 4;
+  const int64_t zero_n4 = (reinterpret_cast<float*>(w) - dk_acc) / 4;
   uint16_t* qh = reinterpret_cast<uint16_t*>(w);
   w += round_up(sizeof(uint16_t) * T * Hq * kHeadDim, 256);
   uint16_t* doh = reinterpret_cast<uint16_t*>(w);
@@ -184,13 +177,14 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
   int32_t* unit_ctr = reinterpret_cast<int32_t*>(w);
 
   // loads: Q/dO boxes of 8 tokens x 16 heads x 64 dims, K/V boxes of 64 keys x 64 dims;
-  // reduce-adds: dQ boxes of 2 tokens x 16 heads x 32 dims, dK/dV of 32 keys x 32 dims (fp32)
+  // reduce-adds: dQ boxes of 2 tokens x 16 heads x 64 dims (bf16, into the output),
+  // dK/dV of 32 keys x 32 dims (fp32)
   CUtensorMap tmQ, tmdO, tmK, tmV, tmdQ, tmdK, tmdV;
   const int64_t Hi = Hq / 16;
   bool ok = make_tmap_3d(&tmQ, qh, false, T * Hi, 16, 64, 16, 8) &&
             make_tmap_3d(&tmdO, doh, false, T * Hi, 16, 64, 16, 8) &&
             make_tmap_3d(&tmK, k, false, W, Hkv, 64, 1, 64) && make_tmap_3d(&tmV, v, false, W, Hkv, 64, 1, 64) &&
-            make_tmap_3d(&tmdQ, dq_acc, true, T * Hi, 16, 32, 16, 2) &&
+            make_tmap_3d(&tmdQ, dq, false, T, Hq, 64, 16, 2) &&
             make_tmap_3d(&tmdK, dk_acc, true, W * Hkv, 1, 32, 1, 32) &&
             make_tmap_3d(&tmdV, dv_acc, true, W * Hkv, 1, 32, 1, 32);
   if (!ok) return MSA_ERR_CUDA;
@@ -200,7 +194,7 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
     preprocess_kernel<<<sms * 8, 256, 0, st>>>(
         reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), reinterpret_cast<const uint4*>(q),
         reinterpret_cast<uint4*>(qh), reinterpret_cast<uint4*>(doh), delta, T, (int)Hq,
-        reinterpret_cast<float4*>(dq_acc), zero_n4, d_status);
+        reinterpret_cast<float4*>(dk_acc), zero_n4, reinterpret_cast<uint4*>(dq), d_status);
   if (stages & MSA_STAGE_MAIN) {
   if (cudaFuncSetAttribute(bwd_main_ws, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ws::SMEM) != cudaSuccess)
     return MSA_ERR_CUDA;
@@ -215,7 +209,6 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
   }
   if (stages & MSA_STAGE_POSTPROCESS)
     postprocess_kernel<<<sms * 8, 256, 0, st>>>(
-      reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<uint4*>(dq), T * Hq * kHeadDim / 8, T, (int)Hq,
       reinterpret_cast<const float4*>(dk_acc), reinterpret_cast<const float4*>(dv_acc), reinterpret_cast<uint4*>(dk),
       reinterpret_cast<uint4*>(dv), W * Hkv * kHeadDim / 8, W, (int)Hkv, p->cu_seqlens,
       p->kv_doc_starts, p->num_docs, d_status);

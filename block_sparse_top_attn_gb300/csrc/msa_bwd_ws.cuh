@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
       uint8_t* stg0 = sm + OFF_ST + (warp - kRed0) * 8192;
       uint32_t chunk = 0;
-      // the dQ accumulator rows of a query chunk take a reduce-add from every
+      // the dQ rows of a query chunk take a reduce-add from every
       // task of the chunk; a dK/dV tile one per bucket segment
       const uint64_t keep = l2_evict_last(), stream = l2_evict_first();
       for (uint32_t j = 0;; ++j) {
@@ -495,34 +495,34 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         if (!wait_bar_warp(sh, DQ_FULL + pb, (j >> 1) & 1, a.status)) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
+        for (int hf = 0; hf < 2; ++hf, ++chunk) {
           uint32_t v[64];
           const uint32_t col = col_dq(pb) + hf * 64;
-          tmem_ld16(tmem + lane_base + col, *reinterpret_cast<uint32_t(*)[16]>(v));
-          tmem_ld16(tmem + lane_base + col + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-          tmem_ld16(tmem + lane_base + col + 32, *reinterpret_cast<uint32_t(*)[16]>(v + 32));
-          tmem_ld16(tmem + lane_base + col + 48, *reinterpret_cast<uint32_t(*)[16]>(v + 48));
+          tmem_ld32x(tmem + lane_base + col, *reinterpret_cast<uint32_t(*)[32]>(v));
+          tmem_ld32x(tmem + lane_base + col + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
           tmem_ld_wait();
           if (hf == 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh->bar[DQ_EMPTY + pb]);
           }
+          // 64 dims of this lane's row as bf16: one 128-byte swizzled row of a
+          // 2-token x 16-head x 64-dim box
+          uint8_t* stg = stg0 + (chunk & 1) * 4096;
+          if (lane == 0) bulk_wait_read_but_one();
+          __syncwarp();
 #pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2, ++chunk) {
-            uint8_t* stg = stg0 + (chunk & 1) * 4096;
-            if (lane == 0) bulk_wait_read_but_one();
-            __syncwarp();
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                  make_uint4(v[q2 * 32 + 4 * c], v[q2 * 32 + 4 * c + 1], v[q2 * 32 + 4 * c + 2], v[q2 * 32 + 4 * c + 3]);
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_reduce_add_3d_hint(&tmdQ, stg, hf * 64 + q2 * 32, 0, hi * a.T + tok0 + 2 * sp, keep);
-              bulk_commit();
-            }
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = make_uint4(
+                pack_bf16x2(__uint_as_float(v[8 * c]), __uint_as_float(v[8 * c + 1])),
+                pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3])),
+                pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5])),
+                pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_3d_hint(&tmdQ, stg, hf * 64, hi * 16, tok0 + 2 * sp, keep);
+            bulk_commit();
           }
         }
         if (flags & 2) {
