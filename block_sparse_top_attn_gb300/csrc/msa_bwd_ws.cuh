@@ -1,6 +1,6 @@
 // Warp-specialised, pipelined main backward kernel (sm_103a).
 //
-// Roles (16 warps, 512 threads, one CTA per SM, persistent over the walk):
+// Roles (24 warps, 768 threads, one CTA per SM, persistent over the walk):
 //   warp 0      task-info producer: walks the CTA's task sequence up to
 //               kInfo tasks ahead and publishes, per task, its index head,
 //               key block, K/V row, token row, query positions and bucket
@@ -14,10 +14,11 @@
 //               each waits on its own dependencies; their TMEM targets are
 //               disjoint and every cross-phase ordering goes through an
 //               mbarrier.
-//   warps 4-11  softmax / dS: TMEM -> registers -> P, dS (bf16, swizzled
+//   warps 4-19  softmax / dS: TMEM -> registers -> P, dS (bf16, swizzled
 //               shared memory).  Warp w owns TMEM lanes 32*(w%4).. and key
-//               columns 32*((w-4)/4)..
-//   warps 12-15 reduce: dQ per task and dK/dV per segment, TMEM -> swizzled
+//               columns 16*((w-4)/4)..; four per SM sub-partition, so the
+//               latency of one warp's exp/convert chain hides behind others'.
+//   warps 20-23 reduce: dQ per task and dK/dV per segment, TMEM -> swizzled
 //               fp32 staging (two 4 KB slots per warp, so a slot is refilled
 //               while the reduce-add of the other is still reading) -> TMA
 //               bulk reduce-add.
@@ -41,9 +42,9 @@
 namespace msa {
 namespace ws {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = 24;
 constexpr int kThreads = kWarps * 32;
-constexpr int kInfoWarp = 0, kLoadWarp = 1, kMmaWarp = 2, kMmaBWarp = 3, kComp0 = 4, kNumComp = 8, kRed0 = 12,
+constexpr int kInfoWarp = 0, kLoadWarp = 1, kMmaWarp = 2, kMmaBWarp = 3, kComp0 = 4, kNumComp = 16, kRed0 = 20,
               kNumRed = 4;
 constexpr int kInfo = 8;  // task-info ring entries
 
@@ -176,13 +177,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&v)[32]) {
   tmem_ld_wait();
 }
 
-// 32 keys of row m (16 packed bf16 pairs) into the 128B-swizzled
-// [128 rows][64 keys] bf16 tile at base; half selects keys 0-31 or 32-63.
-__device__ __forceinline__ void store_row32(uint8_t* base, int m, int half, const uint32_t (&pk)[16]) {
+// 16 keys of row m (8 packed bf16 pairs) into the 128B-swizzled
+// [128 rows][64 keys] bf16 tile at base; qtr selects keys 16*qtr .. 16*qtr+15.
+__device__ __forceinline__ void store_row16(uint8_t* base, int m, int qtr, const uint32_t (&pk)[8]) {
   uint8_t* row = base + m * 128;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const uint32_t o = static_cast<uint32_t>(((half * 4 + c) ^ (m & 7)) << 4);
+  for (int c = 0; c < 2; ++c) {
+    const uint32_t o = static_cast<uint32_t>(((qtr * 2 + c) ^ (m & 7)) << 4);
     *reinterpret_cast<uint4*>(row + o) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
   }
 }
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       }
     } else if (warp < kRed0) {
       // ------------------------------------------------------------ softmax / dS
-      const int sp = warp & 3, half = (warp - kComp0) >> 2;
+      const int sp = warp & 3, qtr = (warp - kComp0) >> 2;
       const int m = sp * 32 + lane, slot_row = m >> 4, hh = m & 15;
       const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
       // Per-row LSE and D of the next task, loaded one task ahead.  The raw
@@ -420,12 +421,12 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           const int nb = ne.b;
           if (nmore) fetch(ne, nqpos, nlse_raw, ndlt_raw);
           const uint32_t par = j & 1;
-          const int kbase = b * 64 + half * 32;
+          const int kbase = b * 64 + qtr * 16;
           if (!wait_bar_warp(sh, S_FULL, par, a.status)) break;
           tc_fence_after();
-          uint32_t sv[32], dpv[32];
-          tmem_ld32x(tmem + lane_base + COL_S + half * 32, sv);
-          tmem_ld32x(tmem + lane_base + COL_DP + half * 32, dpv);
+          uint32_t sv[16], dpv[16];
+          tmem_ld16(tmem + lane_base + COL_S + qtr * 16, sv);
+          tmem_ld16(tmem + lane_base + COL_DP + qtr * 16, dpv);
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
@@ -433,12 +434,12 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           const float lse2 = lse_raw * kLog2e, dsc = dlt_raw * a.scale;
           // P = exp2(S * scale * log2e - LSE * log2e) on the causal mask and
           // dS = P * (dP * scale - D * scale); masked entries are exactly 0
-          uint32_t pk[16], dk[16];
+          uint32_t pk[8], dk[8];
           const int lim = qpos - kbase;  // keys kbase + e with e <= lim are attended
-          if (lim >= 31) {
-            // the whole 32-key slice is attended (every block but the diagonal one)
+          if (lim >= 15) {
+            // the whole 16-key slice is attended (every block but the diagonal one)
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
+            for (int e = 0; e < 16; e += 2) {
               const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), a.scale_log2, -lse2));
               const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), a.scale_log2, -lse2));
               pk[e >> 1] = pack_bf16x2(p0, p1);
@@ -447,7 +448,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
             }
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
+            for (int e = 0; e < 16; e += 2) {
               float p[2], ds[2];
 #pragma unroll
               for (int x = 0; x < 2; ++x) {
@@ -461,8 +462,8 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
             }
           }
           if (!wait_bar_warp(sh, PDS_EMPTY, par ^ 1, a.status)) break;
-          store_row32(sm + OFF_P, m, half, pk);
-          store_row32(sm + OFF_DS, m, half, dk);
+          store_row16(sm + OFF_P, m, qtr, pk);
+          store_row16(sm + OFF_DS, m, qtr, dk);
           fence_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh->bar[PDS_FULL]);
@@ -496,11 +497,17 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         tc_fence_after();
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf, ++chunk) {
-          uint32_t v[64];
-          const uint32_t col = col_dq(pb) + hf * 64;
-          tmem_ld32x(tmem + lane_base + col, *reinterpret_cast<uint32_t(*)[32]>(v));
-          tmem_ld32x(tmem + lane_base + col + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-          tmem_ld_wait();
+          // 64 dims in two 32-column loads, each packed to bf16 on arrival
+          uint32_t pq[32];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t v[32];
+            tmem_ld32x(tmem + lane_base + col_dq(pb) + hf * 64 + h2 * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pq[h2 * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          }
           if (hf == 1) {
             tc_fence_before();
             __syncwarp();
@@ -513,11 +520,8 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           __syncwarp();
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = make_uint4(
-                pack_bf16x2(__uint_as_float(v[8 * c]), __uint_as_float(v[8 * c + 1])),
-                pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3])),
-                pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5])),
-                pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                make_uint4(pq[4 * c], pq[4 * c + 1], pq[4 * c + 2], pq[4 * c + 3]);
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
