@@ -33,17 +33,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
 // preprocess: D[t, h] = sum_d dO * O (fp32), zeroed dK/dV fp32 accumulators and
-// bf16 dQ output, and index-head-major copies of Q and dO for the main kernel.
-//
-// Index-head-major ([Hi][T][16][128]) puts one task's 8 tokens x 16 q-heads in
-// one contiguous block.  In the [T][Hq][128] layout that block is 8 pieces at a
-// stride of Hq x 256 bytes; with many index heads those strided pieces map to
-// few L2 sets and the main kernel's reused tiles keep getting evicted.
+// bf16 dQ output
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
-                                                          const uint4* __restrict__ q, uint4* __restrict__ qh,
-                                                          uint4* __restrict__ doh, float* __restrict__ delta,
-                                                          int64_t T, int Hq, float4* __restrict__ zero,
+                                                          float* __restrict__ delta, int64_t T, int Hq,
+                                                          float4* __restrict__ zero,
                                                           int64_t zero_n4, uint4* __restrict__ dq,
                                                           const int32_t* status) {
   if (status_bad(status)) return;
@@ -55,11 +49,6 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
     float acc = 0.f;
     if (i < total16) {
       const uint4 a = o[i], b = dout[i];
-      const int64_t row = i >> 4, t = row / Hq;
-      const int h = (int)(row - t * Hq);
-      const int64_t dst = ((((int64_t)(h >> 4) * T + t) << 4) + (h & 15)) * 16 + (i & 15);
-      qh[dst] = q[i];
-      doh[dst] = b;
       const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -130,7 +119,6 @@ struct MainArgs {
   const int32_t* walk;
   const int32_t* kv_doc_starts;
   int Hq;
-  int T;              // rows of the token axis (the Q, dO copies are [Hi][T][16][128])
   int W;              // rows of the K/V axis (the dK, dV accumulators are [Hkv][W][128])
   int32_t* unit_ctr;  // next walk unit to hand out; 0 at launch
   float scale_log2;
@@ -170,19 +158,13 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
   float* dv_acc = reinterpret_cast<float*>(w);
   w += round_up(sizeof(float) * W * Hkv * kHeadDim, 256);
   const int64_t zero_n4 = (reinterpret_cast<float*>(w) - dk_acc) / 4;
-  uint16_t* qh = reinterpret_cast<uint16_t*>(w);
-  w += round_up(sizeof(uint16_t) * T * Hq * kHeadDim, 256);
-  uint16_t* doh = reinterpret_cast<uint16_t*>(w);
-  w += round_up(sizeof(uint16_t) * T * Hq * kHeadDim, 256);
   int32_t* unit_ctr = reinterpret_cast<int32_t*>(w);
 
   // loads: Q/dO boxes of 8 tokens x 16 heads x 64 dims, K/V boxes of 64 keys x 64 dims;
   // reduce-adds: dQ boxes of 2 tokens x 16 heads x 64 dims (bf16, into the output),
   // dK/dV of 32 keys x 32 dims (fp32)
   CUtensorMap tmQ, tmdO, tmK, tmV, tmdQ, tmdK, tmdV;
-  const int64_t Hi = Hq / 16;
-  bool ok = make_tmap_3d(&tmQ, qh, false, T * Hi, 16, 64, 16, 8) &&
-            make_tmap_3d(&tmdO, doh, false, T * Hi, 16, 64, 16, 8) &&
+  bool ok = make_tmap_3d(&tmQ, q, false, T, Hq, 64, 16, 8) && make_tmap_3d(&tmdO, dout, false, T, Hq, 64, 16, 8) &&
             make_tmap_3d(&tmK, k, false, W, Hkv, 64, 1, 64) && make_tmap_3d(&tmV, v, false, W, Hkv, 64, 1, 64) &&
             make_tmap_3d(&tmdQ, dq, false, T, Hq, 64, 16, 2) &&
             make_tmap_3d(&tmdK, dk_acc, true, W * Hkv, 1, 32, 1, 32) &&
@@ -192,8 +174,7 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
   if (stages & ~(uint32_t)MSA_STAGE_ALL) return MSA_ERR_INVALID_ARGUMENT;
   if (stages & MSA_STAGE_PREPROCESS)
     preprocess_kernel<<<sms * 8, 256, 0, st>>>(
-        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), reinterpret_cast<const uint4*>(q),
-        reinterpret_cast<uint4*>(qh), reinterpret_cast<uint4*>(doh), delta, T, (int)Hq,
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), delta, T, (int)Hq,
         reinterpret_cast<float4*>(dk_acc), zero_n4, reinterpret_cast<uint4*>(dq), d_status);
   if (stages & MSA_STAGE_MAIN) {
   if (cudaFuncSetAttribute(bwd_main_ws, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ws::SMEM) != cudaSuccess)
@@ -202,7 +183,7 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
   const int grid = (int)(bound < sms ? (bound < 1 ? 1 : bound) : sms);
   MainArgs a;
   a.lse = lse; a.delta = delta; a.meta = task_meta; a.q_rows = task_q_rows; a.q_pos = task_q_pos; a.walk = walk;
-  a.kv_doc_starts = p->kv_doc_starts; a.Hq = (int)Hq; a.T = (int)T; a.W = (int)W; a.unit_ctr = unit_ctr; a.scale_log2 = p->softmax_scale * kLog2e;
+  a.kv_doc_starts = p->kv_doc_starts; a.Hq = (int)Hq; a.W = (int)W; a.unit_ctr = unit_ctr; a.scale_log2 = p->softmax_scale * kLog2e;
   a.scale = p->softmax_scale; a.status = d_status;
   if ((rc = cuda_status(cudaMemsetAsync(unit_ctr, 0, sizeof(int32_t), st)))) return rc;
   bwd_main_ws<<<grid, ws::kThreads, ws::SMEM, st>>>(tmQ, tmdO, tmK, tmV, tmdQ, tmdK, tmdV, a);

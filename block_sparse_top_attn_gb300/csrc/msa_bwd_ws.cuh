@@ -302,13 +302,12 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           uint8_t* st = sm + OFF_QDO + qst * QDO_STAGE;
           if (!wait_bar(sh, Q_EMPTY + qst, qph, a.status)) break;
           mbar_arrive_expect_tx(&sh->bar[Q_FULL + qst], 32768u);
-          const int qrow = hi * a.T + e.tok0;  // Q and dO are index-head-major
-          tma_load_3d_hint(st, &tmQ, &sh->bar[Q_FULL + qst], 0, 0, qrow, keep);
-          tma_load_3d_hint(st + 16384, &tmQ, &sh->bar[Q_FULL + qst], 64, 0, qrow, keep);
+          tma_load_3d_hint(st, &tmQ, &sh->bar[Q_FULL + qst], 0, hi * 16, e.tok0, keep);
+          tma_load_3d_hint(st + 16384, &tmQ, &sh->bar[Q_FULL + qst], 64, hi * 16, e.tok0, keep);
           if (!wait_bar(sh, DO_EMPTY + qst, qph, a.status)) break;
           mbar_arrive_expect_tx(&sh->bar[DO_FULL + qst], 32768u);
-          tma_load_3d_hint(st + DO_IN_STAGE, &tmdO, &sh->bar[DO_FULL + qst], 0, 0, qrow, keep);
-          tma_load_3d_hint(st + DO_IN_STAGE + 16384, &tmdO, &sh->bar[DO_FULL + qst], 64, 0, qrow, keep);
+          tma_load_3d_hint(st + DO_IN_STAGE, &tmdO, &sh->bar[DO_FULL + qst], 0, hi * 16, e.tok0, keep);
+          tma_load_3d_hint(st + DO_IN_STAGE + 16384, &tmdO, &sh->bar[DO_FULL + qst], 64, hi * 16, e.tok0, keep);
         }
       }
     } else if (warp == kMmaWarp || warp == kMmaBWarp) {

@@ -62,7 +62,6 @@ size_t bwd_ws_bytes(const msa_problem* p) {
   const int64_t T = p->total_tokens, Hq = p->num_q_heads, W = p->kv_rows, Hkv = p->num_kv_heads;
   size_t b = round_up(sizeof(float) * T * Hq, 256);                 // D
   b += 2 * round_up(sizeof(float) * W * Hkv * kHeadDim, 256);       // dK, dV accumulators
-  b += 2 * round_up(sizeof(uint16_t) * T * Hq * kHeadDim, 256);     // index-head-major Q, dO
   b += 256;                                                          // walk-unit counter
   return b;
 }
