@@ -48,6 +48,24 @@ def _rank():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's);
+    x itself when the job has one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, flop_per_rank: float, ms: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own batch of flop_per_rank (weak
+    scaling, no data-path collective), the job takes ms."""
+    return world * flop_per_rank / (ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
@@ -274,13 +292,9 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     bw.check_status()
-    ms = t_start.elapsed_time(t_end) / args.steps
+    ms = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, dev)
     main_ms = sum(a.elapsed_time(b) for a, b in main_ev) / args.steps
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    value = world * flop / (ms * 1e-3) / 1e12
+    value = job_value(world, flop, ms)
 
     # end to end through the public API with host buffers (pinned), copies timed
     pin = lambda t: t.cpu().pin_memory()
@@ -313,12 +327,8 @@ def run_gpu(args):
     e1.record(stream)
     torch.cuda.synchronize()
     bw.check_status()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = world * flop / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+    e2e_value = job_value(world, flop, e2e_ms)
 
     burst, sustained, hbm, src = _peaks()
     achieved = flop / (main_ms * 1e-3) / 1e12
