@@ -416,7 +416,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long128k")
-    ap.add_argument("--tile", type=int, default=512, help="query chunks per task tile (0 = untiled)")
+    ap.add_argument("--tile", type=int, default=1024, help="query chunks per task tile (0 = untiled)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -111,7 +111,7 @@ def test_backward_long128k_sampled(B):
         rows = torch.from_numpy(int(lay.cu[0]) + qp).cuda()
         o[rows, hi * G:(hi + 1) * G] = to_bf16_tensor(O.f64_to_bf16(oc.transpose(1, 0, 2)), "cuda")
         lse[rows, hi * G:(hi + 1) * G] = torch.from_numpy(np.ascontiguousarray(lc.T).astype(np.float32)).cuda()
-    bw = B.Backward(prob, task_tile_chunks=512)
+    bw = B.Backward(prob, task_tile_chunks=1024)
     dq, dk, dv = bw.run(t["sel"], t["q"], t["k"], t["v"], o, t["do"], lse)
     torch.cuda.synchronize()
     bw.check_status()

@@ -50,7 +50,7 @@ def _check_tables(B, pb, tile, sms=None):
 @pytest.mark.parametrize("name", ["tiny", "single8k", "varlen32k", "zipf64k", "long128k"])
 def test_tables_bit_exact_named(B, name):
     pb = W.make_problem(name, values=False)
-    tile = 512 if name == "long128k" else 0
+    tile = 1024 if name == "long128k" else 0
     _check_tables(B, pb, tile)
 
 
