@@ -254,8 +254,29 @@ def run_gpu(args):
     if int(st[0].item()) != 0:
         raise B.MSAError(int(st[0].item()), "msa_fwd")
     flop = W.effective_flops(pb)
-    bw = B.Backward(prob, task_tile_chunks=args.tile)
     stream = torch.cuda.current_stream()
+
+    # The forward (the next row on the path: it produces O and LSE) timed on its
+    # own, outside the backward step: CUDA events around msa_fwd after one
+    # warm-up call.  Effective FLOP count: QK^T and PV per selected block, 2/5
+    # of the backward's five GEMMs (the two-pass kernel computes QK^T twice).
+    fwd_out = (torch.empty_like(o), torch.empty_like(lse), torch.zeros(4, dtype=torch.int32, device=dev))
+    fwd_ws = torch.empty(max(256, 8 * (pb.num_docs + 1) + 256), dtype=torch.uint8, device=dev)
+    fwd_runs = 3
+    B.msa_fwd(prob, q, k, v, sel, *fwd_out[:2], fwd_out[2], fwd_ws)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(fwd_runs):
+        B.msa_fwd(prob, q, k, v, sel, *fwd_out[:2], fwd_out[2], fwd_ws)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    if int(fwd_out[2][0].item()) != 0:
+        raise B.MSAError(int(fwd_out[2][0].item()), "msa_fwd")
+    fwd_ms = f0.elapsed_time(f1) / fwd_runs
+    fwd_flop = flop * 2 / 5
+    del fwd_out, fwd_ws
+
+    bw = B.Backward(prob, task_tile_chunks=args.tile)
     nsteps_events = []
 
     def step(ev=None):
@@ -393,6 +414,10 @@ def run_gpu(args):
                 "pipeline": "H2D of step i+1 and D2H of step i-1 overlap step i (two device sets, three streams)",
                 "h2d_gbs": h2d / (h2d_ms * 1e-3) / 1e9, "d2h_gbs": d2h / (d2h_ms * 1e-3) / 1e9},
         "gpu_launches": args.steps * 14,
+        "next_rows": {"forward": {"kernel_ms": fwd_ms, "effective_tflops": fwd_flop / (fwd_ms * 1e-3) / 1e12,
+                                  "frac": fwd_flop / (fwd_ms * 1e-3) / 1e12 / sustained,
+                                  "flop_convention": "QK^T and PV per selected block (2 of the 5 backward GEMMs)",
+                                  "timed": "3 msa_fwd calls after one warm-up, outside the backward step"}},
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -97,20 +97,6 @@ MSA_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-// Warm L2 with a tile (no shared memory written, no completion to wait for).
-MSA_DEV void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-MSA_DEV void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
-      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
 // L2 eviction-priority policies for the cache-hinted TMA forms below: data a
 // kernel reuses many times is loaded / reduced with evict_last, data touched
 // once per use with evict_first, so the streamed traffic does not flush the
@@ -133,12 +119,6 @@ MSA_DEV void tma_load_3d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, 
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
       : "memory");
 }
-MSA_DEV void tma_prefetch_l2_3d_hint(const CUtensorMap* map, int c0, int c1, int c2, uint64_t policy) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile.L2::cache_hint [%0, {%1, %2, %3}], %4;" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-               : "memory");
-}
 MSA_DEV void tma_reduce_add_3d_hint(const CUtensorMap* map, const void* src, int c0, int c1, int c2,
                                     uint64_t policy) {
   asm volatile(
@@ -148,7 +128,6 @@ MSA_DEV void tma_reduce_add_3d_hint(const CUtensorMap* map, const void* src, int
       : "memory");
 }
 MSA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-MSA_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // All but the most recent bulk group have finished reading their sources.
 MSA_DEV void bulk_wait_read_but_one() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 MSA_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
