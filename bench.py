@@ -218,9 +218,10 @@ def kernel_source_sha1() -> str:
     return h.hexdigest()
 
 
-def _traffic_record():
+def _traffic_record(workload: str, tile: int):
     """Per-launch DRAM bytes of the main kernel from the committed ncu summary,
-    valid only while the kernel source it was taken on is unchanged."""
+    valid only for the workload and query tiling it was captured on and while
+    the kernel source it was taken on is unchanged."""
     sha = kernel_source_sha1()
     path = os.path.join(ROOT, "profiles", "bwd_main_long128k.md")
     if not os.path.exists(path):
@@ -228,7 +229,9 @@ def _traffic_record():
     txt = open(path).read()
     m = re.search(r"source_sha1:\s*([0-9a-f]{40})", txt)
     t = re.search(r"traffic_bytes_per_launch_full:\s*([0-9.eE+]+)", txt)
-    if m and t and m.group(1) == sha:
+    w = re.search(r"workload:\s*(\S+)", txt)
+    c = re.search(r"task_tile_chunks:\s*(\d+)", txt)
+    if m and t and w and c and m.group(1) == sha and w.group(1) == workload and int(c.group(1)) == tile:
         return float(t.group(1))
     return None
 
@@ -394,7 +397,7 @@ def run_gpu(args):
 
     burst, sustained, hbm, src = _peaks()
     achieved = flop / (main_ms * 1e-3) / 1e12
-    traffic = _traffic_record()
+    traffic = _traffic_record(args.workload, args.tile)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

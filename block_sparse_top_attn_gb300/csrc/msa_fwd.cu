@@ -1,10 +1,15 @@
 // MSA block-sparse attention forward on sm_103a ("msa_bindings" page,
 // sparse_atten_func, the flat forward): per (index head, query chunk) the 128
 // rows (8 tokens x 16 q-heads) attend the chunk's selected key blocks
-// causally.  Two passes over the selected blocks with tcgen05 GEMMs:
-//   pass 1  S = Q K^T                 -> running max and sum of exp2 (log2 LSE)
-//   pass 2  S = Q K^T, P = exp2(S - LSE), O += P V   (P as bf16 in smem)
-// O is written as bf16 and LSE in natural log, the form the backward consumes.
+// causally, in one pass with an online softmax:
+//   S_j = Q K_j^T (tcgen05, fp32 in TMEM), m = running row max (log2 units),
+//   P_j = exp2(S_j - m) (bf16 in smem), l += rowsum(P_j), O += P_j V_j (TMEM).
+// The running max is moved only when a block raises it by more than kTau
+// (so P stays below 2^kTau); O is then rescaled in TMEM by exp2(m_old - m_new).
+// O = O / l is written as bf16 and LSE = (m + log2 l) ln 2, the form the
+// backward consumes.  S is double-buffered in TMEM so the S GEMM of block j+1
+// runs while block j's softmax does; K and V are double-buffered in smem and
+// loaded a block ahead.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -18,13 +23,18 @@ namespace msa {
 
 namespace fwd {
 constexpr uint32_t OFF_Q = 0;       // [2 halves][128 rows][128 B]
-constexpr uint32_t OFF_K = 32768;   // [2 halves][64 keys][128 B]
-constexpr uint32_t OFF_V = 49152;
-constexpr uint32_t OFF_P = 65536;   // [128 rows][64 keys bf16]
-constexpr uint32_t OFF_BAR = 81920;
-constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+constexpr uint32_t OFF_K = 32768;   // 2 buffers x [2 halves][64 keys][128 B]
+constexpr uint32_t OFF_V = 65536;   // 2 buffers x [2 halves][64 keys][128 B]
+constexpr uint32_t OFF_P = 98304;   // [128 rows][64 keys bf16]
+constexpr uint32_t OFF_BAR = 114688;
+constexpr uint32_t BAR_BYTES = 256;
+// Slack for aligning the dynamic window to 1024 B; two CTAs per SM leave
+// 115,712 B each.  A window that would need more than this is reported.
+constexpr uint32_t ALIGN_SLACK = 768;
+constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + ALIGN_SLACK;
 constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t COL_S = 0, COL_O = 128;
+constexpr uint32_t COL_S = 0, COL_O = 128;  // S buffers at 0 and 64
+constexpr float kTau = 8.f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 }  // namespace fwd
@@ -34,6 +44,20 @@ __device__ __forceinline__ float lg2_approx(float x) {
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+
+// 32 lanes x 32 bit, 32 consecutive columns per thread (thread t -> lane base+t).
+__device__ __forceinline__ void tmem_st32x(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
+      " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16,"
+      " %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 struct FwdArgs {
   const int32_t* sel;
@@ -60,15 +84,29 @@ __global__ void __launch_bounds__(128, 1)
                const __grid_constant__ CUtensorMap tmV, const int32_t* kv_doc_starts, FwdArgs a) {
   using namespace fwd;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bar_load = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  uint64_t* bar_mma = bar_load + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_load + 2);
-  int* s_blocks = reinterpret_cast<int*>(bar_load + 4);  // up to 32 selected blocks
+  const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
+  const uintptr_t pad = ((raw + 1023) & ~uintptr_t(1023)) - raw;
+  if (pad > ALIGN_SLACK) {  // uniform across the block: nothing has started yet
+    if (threadIdx.x == 0) set_status(a.status, MSA_ERR_CUDA);
+    return;
+  }
+  uint8_t* sm = smem_raw + pad;
+  uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint64_t* bar_pv = bar_q + 1;
+  uint64_t* bar_k = bar_q + 2;  // two
+  uint64_t* bar_v = bar_q + 4;  // two
+  uint64_t* bar_s = bar_q + 6;  // two
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 8);
+  int* s_blocks = reinterpret_cast<int*>(bar_q + 10);  // up to 32 selected blocks, count at [32]
   const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
-    mbar_init(bar_load, 1);
-    mbar_init(bar_mma, 1);
+    mbar_init(bar_q, 1);
+    mbar_init(bar_pv, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_k[i], 1);
+      mbar_init(&bar_v[i], 1);
+      mbar_init(&bar_s[i], 1);
+    }
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -83,7 +121,9 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t sbase = smem_u32(sm);
   constexpr uint32_t ID_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t ID_O = idesc_bf16_f32(128, 128, false, true);
-  uint32_t ph_load = 0, ph_mma = 0;
+  // Blocks processed so far by this CTA: block n uses K/V/S buffer n & 1 and
+  // waits phase parity (n >> 1) & 1 on their barriers, parity n & 1 on bar_pv.
+  uint32_t seq = 0, ph_q = 0;
   bool aborted = status_bad(a.status);
   const int64_t items = (int64_t)a.Hi * a.NC;
   for (int64_t w = blockIdx.x; w < items && !aborted; w += gridDim.x) {
@@ -106,124 +146,180 @@ __global__ void __launch_bounds__(128, 1)
     __syncthreads();
     const int nblk = s_blocks[32];
     const int kv0 = kv_doc_starts[d];
+    const uint32_t seq0 = seq;
     float m_run = -CUDART_INF_F, l_run = 0.f;
-    bool q_loaded = false;
-    for (int pass = 0; pass < 2 && !aborted; ++pass) {
-      float lse2 = m_run + lg2_approx(l_run);
-      for (int j = 0; j < nblk; ++j) {
-        const int b = s_blocks[j];
-        const int kvrow = kv0 + b * 64;
-        if (tid == 0) {
-          const uint32_t bytes = (q_loaded ? 0u : 32768u) + 16384u + (pass == 1 ? 16384u : 0u);
-          mbar_arrive_expect_tx(bar_load, bytes);
-          if (!q_loaded) {
-            tma_load_3d(sm + OFF_Q, &tmQ, bar_load, 0, hi * 16, tok0);
-            tma_load_3d(sm + OFF_Q + 16384, &tmQ, bar_load, 64, hi * 16, tok0);
-          }
-          tma_load_3d(sm + OFF_K, &tmK, bar_load, 0, hi, kvrow);
-          tma_load_3d(sm + OFF_K + 8192, &tmK, bar_load, 64, hi, kvrow);
-          if (pass == 1) {
-            tma_load_3d(sm + OFF_V, &tmV, bar_load, 0, hi, kvrow);
-            tma_load_3d(sm + OFF_V + 8192, &tmV, bar_load, 64, hi, kvrow);
-          }
+    // Every MMA of the previous item has completed: all buffers are free.
+    if (tid == 0 && nblk > 0) {
+      mbar_arrive_expect_tx(bar_q, 32768u);
+      tma_load_3d(sm + OFF_Q, &tmQ, bar_q, 0, hi * 16, tok0);
+      tma_load_3d(sm + OFF_Q + 16384, &tmQ, bar_q, 64, hi * 16, tok0);
+      for (int j = 0; j < 2 && j < nblk; ++j) {
+        const uint32_t bf = (seq0 + j) & 1;
+        const int row = kv0 + s_blocks[j] * 64;
+        mbar_arrive_expect_tx(&bar_k[bf], 16384u);
+        tma_load_3d(sm + OFF_K + bf * 16384, &tmK, &bar_k[bf], 0, hi, row);
+        tma_load_3d(sm + OFF_K + bf * 16384 + 8192, &tmK, &bar_k[bf], 64, hi, row);
+        mbar_arrive_expect_tx(&bar_v[bf], 16384u);
+        tma_load_3d(sm + OFF_V + bf * 16384, &tmV, &bar_v[bf], 0, hi, row);
+        tma_load_3d(sm + OFF_V + bf * 16384 + 8192, &tmV, &bar_v[bf], 64, hi, row);
+      }
+      bool ok = mbar_wait(bar_q, ph_q, a.status) && mbar_wait(&bar_k[seq0 & 1], (seq0 >> 1) & 1, a.status);
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
+          umma_bf16(tmem + COL_S + (seq0 & 1) * 64, sdesc_sw128(sbase + OFF_Q + half * 16384 + sub, 16, 1024),
+                    sdesc_sw128(sbase + OFF_K + (seq0 & 1) * 16384 + half * 8192 + sub, 16, 1024), ID_S, kk > 0);
         }
-        q_loaded = true;
-        if (!mbar_wait(bar_load, ph_load, a.status)) aborted = true;
-        ph_load ^= 1;
-        if (__syncthreads_or(aborted)) { aborted = true; break; }
-        if (tid == 0) {
+        umma_commit(&bar_s[seq0 & 1]);
+      } else {
+        aborted = true;
+      }
+    }
+    if (nblk > 0) ph_q ^= 1;
+    for (int j = 0; j < nblk; ++j) {
+      const uint32_t n = seq0 + j, bf = n & 1, par = (n >> 1) & 1;
+      const int b = s_blocks[j];
+      // (1) S_j complete
+      if (!aborted && !mbar_wait(&bar_s[bf], par, a.status)) aborted = true;
+      if (__syncthreads_or(aborted)) { aborted = true; break; }
+      tc_fence_after();
+      // (2) S_{j+1} into the other S buffer (read last by block j-1's softmax,
+      // which finished before the barrier above); K_{j+2} into this K buffer
+      // (its reader S_j has completed)
+      if (tid == 0 && j + 1 < nblk) {
+        const uint32_t n1 = n + 1, b1 = n1 & 1;
+        if (mbar_wait(&bar_k[b1], (n1 >> 1) & 1, a.status)) {
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
-            umma_bf16(tmem + COL_S, sdesc_sw128(sbase + OFF_Q + half * 16384 + sub, 16, 1024),
-                      sdesc_sw128(sbase + OFF_K + half * 8192 + sub, 16, 1024), ID_S, kk > 0);
+            umma_bf16(tmem + COL_S + b1 * 64, sdesc_sw128(sbase + OFF_Q + half * 16384 + sub, 16, 1024),
+                      sdesc_sw128(sbase + OFF_K + b1 * 16384 + half * 8192 + sub, 16, 1024), ID_S, kk > 0);
           }
-          umma_commit(bar_mma);
-        }
-        if (!mbar_wait(bar_mma, ph_mma, a.status)) aborted = true;
-        ph_mma ^= 1;
-        if (__syncthreads_or(aborted)) { aborted = true; break; }
-        tc_fence_after();
-        uint32_t pk[32];
-        float bmax = -CUDART_INF_F;
-        float xs[64];
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-          uint32_t sv[16];
-          tmem_ld16(tmem + lane_base + COL_S + c0, sv);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const bool valid = qpos >= 0 && b * 64 + c0 + e <= qpos;
-            const float x = valid ? __uint_as_float(sv[e]) * a.scale_log2 : -CUDART_INF_F;
-            xs[c0 + e] = x;
-            bmax = fmaxf(bmax, x);
-          }
-        }
-        if (pass == 0) {
-          const float m_new = fmaxf(m_run, bmax);
-          if (m_new > -CUDART_INF_F) {
-            float s = 0.f;
-#pragma unroll
-            for (int e = 0; e < 64; ++e) s += ex2_approx(xs[e] - m_new);
-            l_run = l_run * ex2_approx(m_run - m_new) + s;
-            m_run = m_new;
+          umma_commit(&bar_s[b1]);
+          if (j + 2 < nblk) {
+            const int row = kv0 + s_blocks[j + 2] * 64;
+            mbar_arrive_expect_tx(&bar_k[bf], 16384u);
+            tma_load_3d(sm + OFF_K + bf * 16384, &tmK, &bar_k[bf], 0, hi, row);
+            tma_load_3d(sm + OFF_K + bf * 16384 + 8192, &tmK, &bar_k[bf], 64, hi, row);
           }
         } else {
+          aborted = true;
+        }
+      }
+      // (3) softmax of block j
+      float xs[64];
+      float bmax = -CUDART_INF_F;
 #pragma unroll
-          for (int e = 0; e < 64; e += 2)
-            pk[e >> 1] = pack_bf16x2(xs[e] > -CUDART_INF_F ? ex2_approx(xs[e] - lse2) : 0.f,
-                                     xs[e + 1] > -CUDART_INF_F ? ex2_approx(xs[e + 1] - lse2) : 0.f);
-          uint8_t* prow = sm + OFF_P + tid * 128;
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t sv[32];
+        tmem_ld32x(tmem + lane_base + COL_S + bf * 64 + c0, sv);
+        tmem_ld_wait();
 #pragma unroll
-          for (int cc = 0; cc < 8; ++cc)
-            *reinterpret_cast<uint4*>(prow + ((cc ^ (tid & 7)) << 4)) =
-                make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-          fence_async_smem();
-          tc_fence_before();
-          __syncthreads();
-          if (tid == 0) {
-            tc_fence_after();
+        for (int e = 0; e < 32; ++e) {
+          const bool valid = qpos >= 0 && b * 64 + c0 + e <= qpos;
+          const float x = valid ? __uint_as_float(sv[e]) * a.scale_log2 : -CUDART_INF_F;
+          xs[c0 + e] = x;
+          bmax = fmaxf(bmax, x);
+        }
+      }
+      const bool upd = bmax > m_run + kTau;  // also true for the row's first key
+      const bool resc = upd && m_run > -CUDART_INF_F;
+      const float alpha = upd ? ex2_approx(m_run - bmax) : 1.f;
+      if (upd) {
+        l_run *= alpha;
+        m_run = bmax;
+      }
+      // P_j V_j and the O rescale need P V of block j-1 complete (it reads P
+      // and accumulates O)
+      if (j > 0 && !aborted && !mbar_wait(bar_pv, (n - 1) & 1, a.status)) aborted = true;
+      tc_fence_after();
+      // V_{j+1} into the V buffer that P V of block j-1 read
+      if (tid == 0 && j >= 1 && j + 1 < nblk && !aborted) {
+        const uint32_t b1 = (n + 1) & 1;
+        const int row = kv0 + s_blocks[j + 1] * 64;
+        mbar_arrive_expect_tx(&bar_v[b1], 16384u);
+        tma_load_3d(sm + OFF_V + b1 * 16384, &tmV, &bar_v[b1], 0, hi, row);
+        tma_load_3d(sm + OFF_V + b1 * 16384 + 8192, &tmV, &bar_v[b1], 64, hi, row);
+      }
+      if (__any_sync(0xffffffffu, resc)) {  // warp-collective TMEM access
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld32x(tmem + lane_base + COL_O + c0, ov);
+          tmem_ld_wait();
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(tmem + COL_O, sdesc_sw128(sbase + OFF_P + kk * 32, 16, 1024),
-                        sdesc_sw128(sbase + OFF_V + kk * 2048, 8192, 1024), ID_O, (j > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(bar_mma);
-          }
-          if (!mbar_wait(bar_mma, ph_mma, a.status)) aborted = true;
-          ph_mma ^= 1;
-          if (__syncthreads_or(aborted)) { aborted = true; break; }
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st32x(tmem + lane_base + COL_O + c0, ov);
+        }
+        tmem_st_wait();
+      }
+      uint32_t pk[32];
+      float ls = 0.f;
+#pragma unroll
+      for (int e = 0; e < 64; e += 2) {
+        const float p0 = xs[e] > -CUDART_INF_F ? ex2_approx(xs[e] - m_run) : 0.f;
+        const float p1 = xs[e + 1] > -CUDART_INF_F ? ex2_approx(xs[e + 1] - m_run) : 0.f;
+        ls += p0 + p1;
+        pk[e >> 1] = pack_bf16x2(p0, p1);
+      }
+      l_run += ls;
+      uint8_t* prow = sm + OFF_P + tid * 128;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+        *reinterpret_cast<uint4*>(prow + ((cc ^ (tid & 7)) << 4)) =
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      fence_async_smem();
+      tc_fence_before();
+      if (__syncthreads_or(aborted)) { aborted = true; break; }
+      // (4) O += P_j V_j
+      if (tid == 0) {
+        if (mbar_wait(&bar_v[bf], par, a.status)) {
           tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + COL_O, sdesc_sw128(sbase + OFF_P + kk * 32, 16, 1024),
+                      sdesc_sw128(sbase + OFF_V + bf * 16384 + kk * 2048, 8192, 1024), ID_O,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar_pv);
+        } else {
+          aborted = true;
         }
       }
     }
-    if (aborted) break;
-    // epilogue: O row -> bf16 global, LSE natural log.  TMEM loads are
+    if (nblk > 0 && !aborted) {
+      if (!mbar_wait(bar_pv, (seq0 + nblk - 1) & 1, a.status)) aborted = true;
+    }
+    seq = seq0 + nblk;
+    if (__syncthreads_or(aborted)) break;
+    tc_fence_after();
+    // epilogue: O / l -> bf16 global, LSE natural log.  TMEM loads are
     // warp-collective, so every thread loads and only real rows store.
     {
       const int64_t row = (int64_t)(tok0 + slot) * a.Hq + hi * 16 + hh;
       if (qpos >= 0) a.lse[row] = l_run > 0.f ? (m_run + lg2_approx(l_run)) * kLn2 : -CUDART_INF_F;
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(a.o + row * 128);
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 16) {
-        uint32_t v[16];
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t v[32];
         if (nblk > 0) {
-          tmem_ld16(tmem + lane_base + COL_O + c0, v);
+          tmem_ld32x(tmem + lane_base + COL_O + c0, v);
           tmem_ld_wait();
         } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = 0u;
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
         }
         if (qpos >= 0) {
-          dst[c0 / 8] = make_uint4(pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
-                                   pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
-                                   pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
-                                   pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
-          dst[c0 / 8 + 1] = make_uint4(pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9])),
-                                       pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11])),
-                                       pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13])),
-                                       pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15])));
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            dst[c0 / 8 + q4] = make_uint4(
+                pack_bf16x2(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv),
+                pack_bf16x2(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv),
+                pack_bf16x2(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv),
+                pack_bf16x2(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv));
         }
       }
     }
@@ -267,15 +363,28 @@ extern "C" int msa_fwd(const msa_problem* p, const uint16_t* q, const uint16_t* 
     return MSA_ERR_CUDA;
   layout_kernel<<<1, 1024, 0, st>>>(p->cu_seqlens, p->kv_doc_starts, N, p->total_tokens, p->kv_rows,
                                     p->num_blocks, p->num_chunks, blk_off, chunk_off, d_status);
-  if (cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fwd::SMEM) != cudaSuccess)
+  // The largest shared-memory carveout: two CTAs of ~113 KB share one SM.
+  if (cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fwd::SMEM) != cudaSuccess ||
+      cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     return MSA_ERR_CUDA;
   FwdArgs a;
   a.sel = sel; a.cu = p->cu_seqlens; a.chunk_off = chunk_off; a.o = o; a.lse = lse; a.N = N;
   a.NC = p->num_chunks; a.K = p->topk; a.Hi = p->num_index_heads; a.Hq = (int)Hq;
   a.scale_log2 = p->softmax_scale * fwd::kLog2e; a.status = d_status;
   const int64_t items = (int64_t)p->num_index_heads * p->num_chunks;
-  // ~82 KB of shared memory: two CTAs per SM
-  const int grid = (int)(items < 2 * sms ? items : 2 * sms);
+  // CTAs resident per SM: shared memory per SM over this CTA's share (with
+  // the per-block reservation), at most two (two 256-column TMEM allocations).
+  int dev = 0, smem_sm = 0, smem_rsv = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  int per_sm = smem_sm / ((int)fwd::SMEM + smem_rsv);
+  if (per_sm > 2) per_sm = 2;
+  if (per_sm < 1) return MSA_ERR_CUDA;
+  const int64_t slots = (int64_t)per_sm * sms;
+  const int grid = (int)(items < slots ? items : slots);
   fwd_kernel<<<grid, 128, fwd::SMEM, st>>>(tmQ, tmK, tmV, p->kv_doc_starts, a);
   return cuda_status(cudaGetLastError());
 }
