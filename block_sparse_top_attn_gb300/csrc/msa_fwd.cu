@@ -7,9 +7,13 @@
 // The running max is moved only when a block raises it by more than kTau
 // (so P stays below 2^kTau); O is then rescaled in TMEM by exp2(m_old - m_new).
 // O = O / l is written as bf16 and LSE = (m + log2 l) ln 2, the form the
-// backward consumes.  S is double-buffered in TMEM so the S GEMM of block j+1
-// runs while block j's softmax does; K and V are double-buffered in smem and
-// loaded a block ahead.
+// backward consumes.
+//
+// Warps 0-3 run the softmax, one row per thread; warp 4 loads tiles (TMA) and
+// issues the GEMMs.  They hand off through mbarriers: S_j full (MMA commit),
+// S_j read (softmax), P_j written (softmax), P_j V_j done (MMA commit).  S is
+// double-buffered in TMEM so S_{j+1} is computed while block j's softmax runs;
+// K and V are double-buffered in smem and loaded ahead of their GEMMs.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -22,6 +26,8 @@
 namespace msa {
 
 namespace fwd {
+constexpr int kThreads = 160;       // 4 softmax warps + 1 load/MMA warp
+constexpr int kIssueWarp = 4;
 constexpr uint32_t OFF_Q = 0;       // [2 halves][128 rows][128 B]
 constexpr uint32_t OFF_K = 32768;   // 2 buffers x [2 halves][64 keys][128 B]
 constexpr uint32_t OFF_V = 65536;   // 2 buffers x [2 halves][64 keys][128 B]
@@ -79,7 +85,14 @@ __device__ __forceinline__ int doc_of_chunk(const int32_t* chunk_off, int n, int
   return lo;
 }
 
-__global__ void __launch_bounds__(128, 1)
+// Both halves (64 of the 128 head dims each) of one 64-key K or V block.
+__device__ __forceinline__ void load_kv(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int hi, int row) {
+  mbar_arrive_expect_tx(bar, 16384u);
+  tma_load_3d(dst, map, bar, 0, hi, row);
+  tma_load_3d(dst + 8192, map, bar, 64, hi, row);
+}
+
+__global__ void __launch_bounds__(fwd::kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const int32_t* kv_doc_starts, FwdArgs a) {
   using namespace fwd;
@@ -92,20 +105,24 @@ __global__ void __launch_bounds__(128, 1)
   }
   uint8_t* sm = smem_raw + pad;
   uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  uint64_t* bar_pv = bar_q + 1;
-  uint64_t* bar_k = bar_q + 2;  // two
-  uint64_t* bar_v = bar_q + 4;  // two
-  uint64_t* bar_s = bar_q + 6;  // two
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 8);
-  int* s_blocks = reinterpret_cast<int*>(bar_q + 10);  // up to 32 selected blocks, count at [32]
-  const int tid = threadIdx.x, warp = tid >> 5;
+  uint64_t* bar_pv = bar_q + 1;     // P V done (MMA commit)
+  uint64_t* bar_pfull = bar_q + 2;  // P written, O rescaled (4 softmax warps)
+  uint64_t* bar_k = bar_q + 3;      // two
+  uint64_t* bar_v = bar_q + 5;      // two
+  uint64_t* bar_s = bar_q + 7;      // two: S full (MMA commit)
+  uint64_t* bar_sfree = bar_q + 9;  // two: S read (4 softmax warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 11);
+  int* s_blocks = reinterpret_cast<int*>(bar_q + 12);  // up to 32 selected blocks, count at [32]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     mbar_init(bar_q, 1);
     mbar_init(bar_pv, 1);
+    mbar_init(bar_pfull, 4);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_k[i], 1);
       mbar_init(&bar_v[i], 1);
       mbar_init(&bar_s[i], 1);
+      mbar_init(&bar_sfree[i], 4);
     }
     fence_mbar_init();
   }
@@ -117,214 +134,231 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t sbase = smem_u32(sm);
   constexpr uint32_t ID_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t ID_O = idesc_bf16_f32(128, 128, false, true);
   // Blocks processed so far by this CTA: block n uses K/V/S buffer n & 1 and
-  // waits phase parity (n >> 1) & 1 on their barriers, parity n & 1 on bar_pv.
+  // phase parity (n >> 1) & 1 of their barriers, parity n & 1 of bar_pv and
+  // bar_pfull.
   uint32_t seq = 0, ph_q = 0;
   bool aborted = status_bad(a.status);
   const int64_t items = (int64_t)a.Hi * a.NC;
-  for (int64_t w = blockIdx.x; w < items && !aborted; w += gridDim.x) {
+  for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
     const int hi = (int)(w / a.NC), g = (int)(w % a.NC);
     const int d = doc_of_chunk(a.chunk_off, a.N + 1, g);
-    const int c = g - a.chunk_off[d];
-    const int len = a.cu[d + 1] - a.cu[d];
-    const int tok0 = a.cu[d] + c * 8;
-    const int qcount = min(8, len - c * 8);
-    const int slot = tid >> 4, hh = tid & 15;
-    const int qpos = slot < qcount ? c * 8 + slot : -1;
-    if (tid == 0) {
-      int nb = 0;
-      for (int j = 0; j < a.K; ++j) {
-        const int b = a.sel[((int64_t)hi * a.NC + g) * a.K + j];
-        if (b >= 0) s_blocks[nb++] = b;
-      }
-      s_blocks[32] = nb;
+    if (warp == kIssueWarp) {  // compact the item's selection, order kept
+      const int b = lane < a.K ? a.sel[((int64_t)hi * a.NC + g) * a.K + lane] : -1;
+      const uint32_t m = __ballot_sync(0xffffffffu, b >= 0);
+      if (b >= 0) s_blocks[__popc(m & ((1u << lane) - 1u))] = b;
+      if (lane == 0) s_blocks[32] = __popc(m);
     }
-    __syncthreads();
+    if (__syncthreads_or(aborted)) break;
     const int nblk = s_blocks[32];
     const int kv0 = kv_doc_starts[d];
     const uint32_t seq0 = seq;
-    float m_run = -CUDART_INF_F, l_run = 0.f;
-    // Every MMA of the previous item has completed: all buffers are free.
-    if (tid == 0 && nblk > 0) {
-      mbar_arrive_expect_tx(bar_q, 32768u);
-      tma_load_3d(sm + OFF_Q, &tmQ, bar_q, 0, hi * 16, tok0);
-      tma_load_3d(sm + OFF_Q + 16384, &tmQ, bar_q, 64, hi * 16, tok0);
-      for (int j = 0; j < 2 && j < nblk; ++j) {
-        const uint32_t bf = (seq0 + j) & 1;
-        const int row = kv0 + s_blocks[j] * 64;
-        mbar_arrive_expect_tx(&bar_k[bf], 16384u);
-        tma_load_3d(sm + OFF_K + bf * 16384, &tmK, &bar_k[bf], 0, hi, row);
-        tma_load_3d(sm + OFF_K + bf * 16384 + 8192, &tmK, &bar_k[bf], 64, hi, row);
-        mbar_arrive_expect_tx(&bar_v[bf], 16384u);
-        tma_load_3d(sm + OFF_V + bf * 16384, &tmV, &bar_v[bf], 0, hi, row);
-        tma_load_3d(sm + OFF_V + bf * 16384 + 8192, &tmV, &bar_v[bf], 64, hi, row);
-      }
-      bool ok = mbar_wait(bar_q, ph_q, a.status) && mbar_wait(&bar_k[seq0 & 1], (seq0 >> 1) & 1, a.status);
-      if (ok) {
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
-          umma_bf16(tmem + COL_S + (seq0 & 1) * 64, sdesc_sw128(sbase + OFF_Q + half * 16384 + sub, 16, 1024),
-                    sdesc_sw128(sbase + OFF_K + (seq0 & 1) * 16384 + half * 8192 + sub, 16, 1024), ID_S, kk > 0);
+    if (warp == kIssueWarp) {
+      // ---------------- loads and GEMMs ----------------
+      // Every MMA of the previous item has completed: all buffers are free.
+      if (nblk > 0) {
+        const int c = g - a.chunk_off[d];
+        const int tok0 = a.cu[d] + c * 8;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(bar_q, 32768u);
+          tma_load_3d(sm + OFF_Q, &tmQ, bar_q, 0, hi * 16, tok0);
+          tma_load_3d(sm + OFF_Q + 16384, &tmQ, bar_q, 64, hi * 16, tok0);
+          for (int j = 0; j < 2 && j < nblk; ++j) {
+            const uint32_t bf = (seq0 + j) & 1;
+            load_kv(sm + OFF_K + bf * 16384, &tmK, &bar_k[bf], hi, kv0 + s_blocks[j] * 64);
+            load_kv(sm + OFF_V + bf * 16384, &tmV, &bar_v[bf], hi, kv0 + s_blocks[j] * 64);
+          }
         }
-        umma_commit(&bar_s[seq0 & 1]);
-      } else {
-        aborted = true;
-      }
-    }
-    if (nblk > 0) ph_q ^= 1;
-    for (int j = 0; j < nblk; ++j) {
-      const uint32_t n = seq0 + j, bf = n & 1, par = (n >> 1) & 1;
-      const int b = s_blocks[j];
-      // (1) S_j complete
-      if (!aborted && !mbar_wait(&bar_s[bf], par, a.status)) aborted = true;
-      if (__syncthreads_or(aborted)) { aborted = true; break; }
-      tc_fence_after();
-      // (2) S_{j+1} into the other S buffer (read last by block j-1's softmax,
-      // which finished before the barrier above); K_{j+2} into this K buffer
-      // (its reader S_j has completed)
-      if (tid == 0 && j + 1 < nblk) {
-        const uint32_t n1 = n + 1, b1 = n1 & 1;
-        if (mbar_wait(&bar_k[b1], (n1 >> 1) & 1, a.status)) {
+        __syncwarp();
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, ph_q, a.status) &&
+                                              mbar_wait(&bar_k[seq0 & 1], (seq0 >> 1) & 1, a.status));
+        ph_q ^= 1;
+        if (ok) {
           tc_fence_after();
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
-            umma_bf16(tmem + COL_S + b1 * 64, sdesc_sw128(sbase + OFF_Q + half * 16384 + sub, 16, 1024),
-                      sdesc_sw128(sbase + OFF_K + b1 * 16384 + half * 8192 + sub, 16, 1024), ID_S, kk > 0);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
+              umma_bf16(tmem + COL_S + (seq0 & 1) * 64, sdesc_sw128(sbase + OFF_Q + half * 16384 + sub, 16, 1024),
+                        sdesc_sw128(sbase + OFF_K + (seq0 & 1) * 16384 + half * 8192 + sub, 16, 1024), ID_S,
+                        kk > 0);
+            }
+            umma_commit(&bar_s[seq0 & 1]);
           }
-          umma_commit(&bar_s[b1]);
+          __syncwarp();
+        }
+        for (int j = 0; j < nblk && ok; ++j) {
+          const uint32_t n = seq0 + j, bf = n & 1;
+          // S_{j+1} once K_{j+1} has landed and block j-1's softmax has read
+          // the S buffer it goes into
+          if (j + 1 < nblk) {
+            const uint32_t n1 = n + 1, b1 = n1 & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar_k[b1], (n1 >> 1) & 1, a.status) &&
+                                             (j == 0 || mbar_wait(&bar_sfree[b1], ((n - 1) >> 1) & 1, a.status)));
+            if (!ok) break;
+            tc_fence_after();
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
+                umma_bf16(tmem + COL_S + b1 * 64, sdesc_sw128(sbase + OFF_Q + half * 16384 + sub, 16, 1024),
+                          sdesc_sw128(sbase + OFF_K + b1 * 16384 + half * 8192 + sub, 16, 1024), ID_S, kk > 0);
+              }
+              umma_commit(&bar_s[b1]);
+            }
+            __syncwarp();
+          }
+          // K_{j+2} into this K buffer once S_j (its reader) has completed
           if (j + 2 < nblk) {
-            const int row = kv0 + s_blocks[j + 2] * 64;
-            mbar_arrive_expect_tx(&bar_k[bf], 16384u);
-            tma_load_3d(sm + OFF_K + bf * 16384, &tmK, &bar_k[bf], 0, hi, row);
-            tma_load_3d(sm + OFF_K + bf * 16384 + 8192, &tmK, &bar_k[bf], 64, hi, row);
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[bf], (n >> 1) & 1, a.status)))) break;
+            if (elect_one()) load_kv(sm + OFF_K + bf * 16384, &tmK, &bar_k[bf], hi, kv0 + s_blocks[j + 2] * 64);
+            __syncwarp();
           }
-        } else {
-          aborted = true;
-        }
-      }
-      // (3) softmax of block j
-      float xs[64];
-      float bmax = -CUDART_INF_F;
+          // V_{j+1} into the other V buffer once P V of block j-1 has completed
+          if (j >= 1 && j + 1 < nblk) {
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (n - 1) & 1, a.status)))) break;
+            if (elect_one())
+              load_kv(sm + OFF_V + (bf ^ 1) * 16384, &tmV, &bar_v[bf ^ 1], hi, kv0 + s_blocks[j + 1] * 64);
+            __syncwarp();
+          }
+          // O += P_j V_j once P_j is written and V_j has landed
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(bar_pfull, n & 1, a.status) && mbar_wait(&bar_v[bf], (n >> 1) & 1, a.status));
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) {
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t sv[32];
-        tmem_ld32x(tmem + lane_base + COL_S + bf * 64 + c0, sv);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const bool valid = qpos >= 0 && b * 64 + c0 + e <= qpos;
-          const float x = valid ? __uint_as_float(sv[e]) * a.scale_log2 : -CUDART_INF_F;
-          xs[c0 + e] = x;
-          bmax = fmaxf(bmax, x);
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tmem + COL_O, sdesc_sw128(sbase + OFF_P + kk * 32, 16, 1024),
+                        sdesc_sw128(sbase + OFF_V + bf * 16384 + kk * 2048, 8192, 1024), ID_O,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(bar_pv);
+          }
+          __syncwarp();
         }
+        if (!ok) aborted = true;
       }
-      const bool upd = bmax > m_run + kTau;  // also true for the row's first key
-      const bool resc = upd && m_run > -CUDART_INF_F;
-      const float alpha = upd ? ex2_approx(m_run - bmax) : 1.f;
-      if (upd) {
-        l_run *= alpha;
-        m_run = bmax;
-      }
-      // P_j V_j and the O rescale need P V of block j-1 complete (it reads P
-      // and accumulates O)
-      if (j > 0 && !aborted && !mbar_wait(bar_pv, (n - 1) & 1, a.status)) aborted = true;
-      tc_fence_after();
-      // V_{j+1} into the V buffer that P V of block j-1 read
-      if (tid == 0 && j >= 1 && j + 1 < nblk && !aborted) {
-        const uint32_t b1 = (n + 1) & 1;
-        const int row = kv0 + s_blocks[j + 1] * 64;
-        mbar_arrive_expect_tx(&bar_v[b1], 16384u);
-        tma_load_3d(sm + OFF_V + b1 * 16384, &tmV, &bar_v[b1], 0, hi, row);
-        tma_load_3d(sm + OFF_V + b1 * 16384 + 8192, &tmV, &bar_v[b1], 64, hi, row);
-      }
-      if (__any_sync(0xffffffffu, resc)) {  // warp-collective TMEM access
-#pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t ov[32];
-          tmem_ld32x(tmem + lane_base + COL_O + c0, ov);
+    } else {
+      // ---------------- softmax, one row per thread ----------------
+      const int c = g - a.chunk_off[d];
+      const int len = a.cu[d + 1] - a.cu[d];
+      const int tok0 = a.cu[d] + c * 8;
+      const int qcount = min(8, len - c * 8);
+      const int slot = tid >> 4, hh = tid & 15;
+      const int qpos = slot < qcount ? c * 8 + slot : -1;
+      float m_run = -CUDART_INF_F, l_run = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nblk; ++j) {
+        const uint32_t n = seq0 + j, bf = n & 1;
+        const int b = s_blocks[j];
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[bf], (n >> 1) & 1, a.status));
+        if (!ok) break;
+        tc_fence_after();
+        float xs[64];
+        float bmax = -CUDART_INF_F;
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t sv[32];
+          tmem_ld32x(tmem + lane_base + COL_S + bf * 64 + c0, sv);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st32x(tmem + lane_base + COL_O + c0, ov);
+          for (int e = 0; e < 32; ++e) {
+            const bool valid = qpos >= 0 && b * 64 + c0 + e <= qpos;
+            const float x = valid ? __uint_as_float(sv[e]) * a.scale_log2 : -CUDART_INF_F;
+            xs[c0 + e] = x;
+            bmax = fmaxf(bmax, x);
+          }
         }
-        tmem_st_wait();
-      }
-      uint32_t pk[32];
-      float ls = 0.f;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_sfree[bf]);
+        const bool upd = bmax > m_run + kTau;  // also true for the row's first key
+        const bool resc = upd && m_run > -CUDART_INF_F;
+        const float alpha = upd ? ex2_approx(m_run - bmax) : 1.f;
+        if (upd) {
+          l_run *= alpha;
+          m_run = bmax;
+        }
+        uint32_t pk[32];
+        float ls = 0.f;
 #pragma unroll
-      for (int e = 0; e < 64; e += 2) {
-        const float p0 = xs[e] > -CUDART_INF_F ? ex2_approx(xs[e] - m_run) : 0.f;
-        const float p1 = xs[e + 1] > -CUDART_INF_F ? ex2_approx(xs[e + 1] - m_run) : 0.f;
-        ls += p0 + p1;
-        pk[e >> 1] = pack_bf16x2(p0, p1);
-      }
-      l_run += ls;
-      uint8_t* prow = sm + OFF_P + tid * 128;
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        *reinterpret_cast<uint4*>(prow + ((cc ^ (tid & 7)) << 4)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      fence_async_smem();
-      tc_fence_before();
-      if (__syncthreads_or(aborted)) { aborted = true; break; }
-      // (4) O += P_j V_j
-      if (tid == 0) {
-        if (mbar_wait(&bar_v[bf], par, a.status)) {
+        for (int e = 0; e < 64; e += 2) {
+          const float p0 = xs[e] > -CUDART_INF_F ? ex2_approx(xs[e] - m_run) : 0.f;
+          const float p1 = xs[e + 1] > -CUDART_INF_F ? ex2_approx(xs[e + 1] - m_run) : 0.f;
+          ls += p0 + p1;
+          pk[e >> 1] = pack_bf16x2(p0, p1);
+        }
+        l_run += ls;
+        // P V of block j-1 has read P and accumulated O
+        if (j > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (n - 1) & 1, a.status));
+          if (!ok) break;
           tc_fence_after();
+        }
+        if (__any_sync(0xffffffffu, resc)) {  // warp-collective TMEM access
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t ov[32];
+            tmem_ld32x(tmem + lane_base + COL_O + c0, ov);
+            tmem_ld_wait();
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + COL_O, sdesc_sw128(sbase + OFF_P + kk * 32, 16, 1024),
-                      sdesc_sw128(sbase + OFF_V + bf * 16384 + kk * 2048, 8192, 1024), ID_O,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar_pv);
-        } else {
-          aborted = true;
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32x(tmem + lane_base + COL_O + c0, ov);
+          }
+          tmem_st_wait();
+        }
+        uint8_t* prow = sm + OFF_P + tid * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4*>(prow + ((cc ^ (tid & 7)) << 4)) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_pfull);
+      }
+      if (ok && nblk > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (seq0 + nblk - 1) & 1, a.status));
+      if (!ok) {
+        aborted = true;
+      } else {
+        tc_fence_after();
+        // epilogue: O / l -> bf16 global, LSE natural log.  TMEM loads are
+        // warp-collective, so every thread loads and only real rows store.
+        const int64_t row = (int64_t)(tok0 + slot) * a.Hq + hi * 16 + hh;
+        if (qpos >= 0) a.lse[row] = l_run > 0.f ? (m_run + lg2_approx(l_run)) * kLn2 : -CUDART_INF_F;
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(a.o + row * 128);
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t v[32];
+          if (nblk > 0) {
+            tmem_ld32x(tmem + lane_base + COL_O + c0, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0u;
+          }
+          if (qpos >= 0) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              dst[c0 / 8 + q4] = make_uint4(
+                  pack_bf16x2(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv),
+                  pack_bf16x2(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv),
+                  pack_bf16x2(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv),
+                  pack_bf16x2(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv));
+          }
         }
       }
-    }
-    if (nblk > 0 && !aborted) {
-      if (!mbar_wait(bar_pv, (seq0 + nblk - 1) & 1, a.status)) aborted = true;
     }
     seq = seq0 + nblk;
+    // all of the item's MMAs have completed and its O has been read
+    tc_fence_before();
     if (__syncthreads_or(aborted)) break;
     tc_fence_after();
-    // epilogue: O / l -> bf16 global, LSE natural log.  TMEM loads are
-    // warp-collective, so every thread loads and only real rows store.
-    {
-      const int64_t row = (int64_t)(tok0 + slot) * a.Hq + hi * 16 + hh;
-      if (qpos >= 0) a.lse[row] = l_run > 0.f ? (m_run + lg2_approx(l_run)) * kLn2 : -CUDART_INF_F;
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(a.o + row * 128);
-#pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t v[32];
-        if (nblk > 0) {
-          tmem_ld32x(tmem + lane_base + COL_O + c0, v);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = 0u;
-        }
-        if (qpos >= 0) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            dst[c0 / 8 + q4] = make_uint4(
-                pack_bf16x2(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv),
-                pack_bf16x2(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv),
-                pack_bf16x2(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv),
-                pack_bf16x2(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv));
-        }
-      }
-    }
-    tc_fence_before();
-    __syncthreads();
   }
   tc_fence_before();
   __syncthreads();
@@ -385,6 +419,6 @@ extern "C" int msa_fwd(const msa_problem* p, const uint16_t* q, const uint16_t* 
   if (per_sm < 1) return MSA_ERR_CUDA;
   const int64_t slots = (int64_t)per_sm * sms;
   const int grid = (int)(items < slots ? items : slots);
-  fwd_kernel<<<grid, 128, fwd::SMEM, st>>>(tmQ, tmK, tmV, p->kv_doc_starts, a);
+  fwd_kernel<<<grid, fwd::kThreads, fwd::SMEM, st>>>(tmQ, tmK, tmV, p->kv_doc_starts, a);
   return cuda_status(cudaGetLastError());
 }

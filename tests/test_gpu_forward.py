@@ -35,3 +35,46 @@ def test_forward_matches_oracle(B, case):
     assert_grad_close("o", from_bf16_tensor(o), ro)
     gl = lse.cpu().numpy().astype(np.float64)
     assert np.max(np.abs(gl - rl)) < 2e-3
+
+
+@pytest.mark.parametrize("case", ["empty_chunks", "single_tokens", "topk1", "tail_T", "zipf_shuffled"])
+def test_forward_edge_cases(B, case):
+    """Chunks with no selected block (O = 0, LSE = -inf), -1 pads and blocks in
+    any slot order, one-token documents, top-k 1, a partial last chunk, and a
+    zipf selection whose block order is shuffled so the running max moves."""
+    import torch
+    rng = np.random.default_rng(11)
+    if case == "empty_chunks":
+        pb = W.make_problem(lengths=[300, 260], num_index_heads=2, topk=3, policy="diag_uniform", seed=4)
+        sel = pb.sel.copy()
+        for hi in range(sel.shape[0]):
+            for g in range(sel.shape[1]):
+                sel[hi, g] = sel[hi, g][rng.permutation(sel.shape[2])]
+                if rng.random() < 0.1:
+                    sel[hi, g] = -1
+        pb.sel = sel
+    elif case == "single_tokens":
+        pb = W.make_problem(lengths=[1, 1, 2, 1, 3], num_index_heads=1, topk=2, policy="diag_uniform", seed=2)
+    elif case == "topk1":
+        pb = W.make_problem(lengths=[64 * 5 + 3], num_index_heads=1, topk=1, policy="diag_uniform", seed=3)
+    elif case == "tail_T":
+        pb = W.make_problem(lengths=[555], num_index_heads=1, topk=5, policy="diag_recent3_uniform", seed=5)
+    else:
+        pb = W.make_problem(lengths=[4096, 1500], num_index_heads=2, topk=16, policy="zipf", seed=6)
+        sel = pb.sel.copy()
+        for hi in range(sel.shape[0]):
+            for g in range(sel.shape[1]):
+                sel[hi, g] = sel[hi, g][rng.permutation(sel.shape[2])]
+        pb.sel = sel
+    prob, t = upload(pb)
+    o, lse, st = B.forward(prob, t["sel"], t["q"], t["k"], t["v"])
+    torch.cuda.synchronize()
+    assert int(st[0].item()) == 0
+    ro, rl = O.forward_blocked(pb.q, pb.k, pb.v, pb.cu_seqlens, pb.kv_doc_starts, pb.sel, pb.block, pb.chunk,
+                               pb.softmax_scale)
+    assert_grad_close("o", from_bf16_tensor(o), ro)
+    gl = lse.cpu().numpy().astype(np.float64)
+    empty = ~np.isfinite(rl)
+    assert np.array_equal(empty, ~np.isfinite(gl))          # exactly the rows with no key
+    assert np.all(from_bf16_tensor(o)[empty] == 0)
+    assert np.max(np.abs(gl[~empty] - rl[~empty])) < 2e-3
