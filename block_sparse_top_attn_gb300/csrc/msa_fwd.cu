@@ -3,7 +3,8 @@
 // rows (8 tokens x 16 q-heads) attend the chunk's selected key blocks
 // causally, in one pass with an online softmax:
 //   S_j = Q K_j^T (tcgen05, fp32 in TMEM), m = running row max (log2 units),
-//   P_j = exp2(S_j - m) (bf16 in smem), l += rowsum(P_j), O += P_j V_j (TMEM).
+//   P_j = exp2(S_j - m) (bf16, in TMEM over the columns of S_j),
+//   l += rowsum(P_j), O += P_j V_j (TMEM, the GEMM reads P_j from TMEM).
 // The running max is moved only when a block raises it by more than kTau
 // (so P stays below 2^kTau); O is then rescaled in TMEM by exp2(m_old - m_new).
 // O = O / l is written as bf16 and LSE = (m + log2 l) ln 2, the form the
@@ -11,9 +12,9 @@
 //
 // Warps 0-3 run the softmax, one row per thread; warp 4 loads tiles (TMA) and
 // issues the GEMMs.  They hand off through mbarriers: S_j full (MMA commit),
-// S_j read (softmax), P_j written (softmax), P_j V_j done (MMA commit).  S is
-// double-buffered in TMEM so S_{j+1} is computed while block j's softmax runs;
-// K and V are double-buffered in smem and loaded ahead of their GEMMs.
+// P_j written (softmax), P_j V_j done (MMA commit).  S/P is double-buffered in
+// TMEM: S_{j+1} is computed while block j's softmax runs, once P_{j-1} V_{j-1}
+// has read the buffer.  K and V are double-buffered in smem and loaded ahead.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -31,15 +32,14 @@ constexpr int kIssueWarp = 4;
 constexpr uint32_t OFF_Q = 0;       // [2 halves][128 rows][128 B]
 constexpr uint32_t OFF_K = 32768;   // 2 buffers x [2 halves][64 keys][128 B]
 constexpr uint32_t OFF_V = 65536;   // 2 buffers x [2 halves][64 keys][128 B]
-constexpr uint32_t OFF_P = 98304;   // [128 rows][64 keys bf16]
-constexpr uint32_t OFF_BAR = 114688;
+constexpr uint32_t OFF_BAR = 98304;
 constexpr uint32_t BAR_BYTES = 256;
-// Slack for aligning the dynamic window to 1024 B; two CTAs per SM leave
-// 115,712 B each.  A window that would need more than this is reported.
+// Slack for aligning the dynamic window to 1024 B.  A window that would need
+// more than this is reported.
 constexpr uint32_t ALIGN_SLACK = 768;
 constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + ALIGN_SLACK;
 constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t COL_S = 0, COL_O = 128;  // S buffers at 0 and 64
+constexpr uint32_t COL_S = 0, COL_O = 128;  // S/P buffers at 0 and 64 (P: first 32 columns)
 constexpr float kTau = 8.f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -64,6 +64,18 @@ __device__ __forceinline__ void tmem_st32x(uint32_t taddr, const uint32_t (&r)[3
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem], bf16 inputs, fp32 accumulate.  A is M rows
+// on TMEM lanes, K-major, two bf16 per 32-bit column (lower k in the low half).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 struct FwdArgs {
   const int32_t* sel;
@@ -106,23 +118,23 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
   uint8_t* sm = smem_raw + pad;
   uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* bar_pv = bar_q + 1;     // P V done (MMA commit)
-  uint64_t* bar_pfull = bar_q + 2;  // P written, O rescaled (4 softmax warps)
-  uint64_t* bar_k = bar_q + 3;      // two
-  uint64_t* bar_v = bar_q + 5;      // two
-  uint64_t* bar_s = bar_q + 7;      // two: S full (MMA commit)
-  uint64_t* bar_sfree = bar_q + 9;  // two: S read (4 softmax warps)
+  uint64_t* bar_k = bar_q + 2;      // two
+  uint64_t* bar_v = bar_q + 4;      // two
+  uint64_t* bar_s = bar_q + 6;      // two: S full (MMA commit)
+  // two: P written and O rescaled (4 softmax warps).  One per S/P buffer:
+  // block j+1's softmax may finish before the issuer has waited for block j's.
+  uint64_t* bar_pfull = bar_q + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 11);
   int* s_blocks = reinterpret_cast<int*>(bar_q + 12);  // up to 32 selected blocks, count at [32]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     mbar_init(bar_q, 1);
     mbar_init(bar_pv, 1);
-    mbar_init(bar_pfull, 4);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_k[i], 1);
       mbar_init(&bar_v[i], 1);
       mbar_init(&bar_s[i], 1);
-      mbar_init(&bar_sfree[i], 4);
+      mbar_init(&bar_pfull[i], 4);
     }
     fence_mbar_init();
   }
@@ -138,9 +150,8 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
   const uint32_t sbase = smem_u32(sm);
   constexpr uint32_t ID_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t ID_O = idesc_bf16_f32(128, 128, false, true);
-  // Blocks processed so far by this CTA: block n uses K/V/S buffer n & 1 and
-  // phase parity (n >> 1) & 1 of their barriers, parity n & 1 of bar_pv and
-  // bar_pfull.
+  // Blocks processed so far by this CTA: block n uses K/V/S/P buffer n & 1 and
+  // phase parity (n >> 1) & 1 of their barriers, parity n & 1 of bar_pv.
   uint32_t seq = 0, ph_q = 0;
   bool aborted = status_bad(a.status);
   const int64_t items = (int64_t)a.Hi * a.NC;
@@ -193,12 +204,12 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
         }
         for (int j = 0; j < nblk && ok; ++j) {
           const uint32_t n = seq0 + j, bf = n & 1;
-          // S_{j+1} once K_{j+1} has landed and block j-1's softmax has read
-          // the S buffer it goes into
+          // S_{j+1} once K_{j+1} has landed and P V of block j-1 has read the
+          // S/P buffer it goes into (block j-1's softmax wrote P before that)
           if (j + 1 < nblk) {
             const uint32_t n1 = n + 1, b1 = n1 & 1;
             ok = __all_sync(0xffffffffu, mbar_wait(&bar_k[b1], (n1 >> 1) & 1, a.status) &&
-                                             (j == 0 || mbar_wait(&bar_sfree[b1], ((n - 1) >> 1) & 1, a.status)));
+                                             (j == 0 || mbar_wait(bar_pv, (n - 1) & 1, a.status)));
             if (!ok) break;
             tc_fence_after();
             if (elect_one()) {
@@ -218,24 +229,24 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
             if (elect_one()) load_kv(sm + OFF_K + bf * 16384, &tmK, &bar_k[bf], hi, kv0 + s_blocks[j + 2] * 64);
             __syncwarp();
           }
-          // V_{j+1} into the other V buffer once P V of block j-1 has completed
+          // V_{j+1} into the other V buffer (P V of block j-1 has completed: waited above)
           if (j >= 1 && j + 1 < nblk) {
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (n - 1) & 1, a.status)))) break;
             if (elect_one())
               load_kv(sm + OFF_V + (bf ^ 1) * 16384, &tmV, &bar_v[bf ^ 1], hi, kv0 + s_blocks[j + 1] * 64);
             __syncwarp();
           }
           // O += P_j V_j once P_j is written and V_j has landed
           ok = __all_sync(0xffffffffu,
-                          mbar_wait(bar_pfull, n & 1, a.status) && mbar_wait(&bar_v[bf], (n >> 1) & 1, a.status));
+                          mbar_wait(&bar_pfull[bf], (n >> 1) & 1, a.status) &&
+                              mbar_wait(&bar_v[bf], (n >> 1) & 1, a.status));
           if (!ok) break;
           tc_fence_after();
           if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(tmem + COL_O, sdesc_sw128(sbase + OFF_P + kk * 32, 16, 1024),
-                        sdesc_sw128(sbase + OFF_V + bf * 16384 + kk * 2048, 8192, 1024), ID_O,
-                        (j > 0 || kk > 0) ? 1u : 0u);
+              umma_bf16_ts(tmem + COL_O, tmem + COL_S + bf * 64 + kk * 8,
+                           sdesc_sw128(sbase + OFF_V + bf * 16384 + kk * 2048, 8192, 1024), ID_O,
+                           (j > 0 || kk > 0) ? 1u : 0u);
             umma_commit(bar_pv);
           }
           __syncwarp();
@@ -273,9 +284,6 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
             bmax = fmaxf(bmax, x);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_sfree[bf]);
         const bool upd = bmax > m_run + kTau;  // also true for the row's first key
         const bool resc = upd && m_run > -CUDART_INF_F;
         const float alpha = upd ? ex2_approx(m_run - bmax) : 1.f;
@@ -293,13 +301,11 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
           pk[e >> 1] = pack_bf16x2(p0, p1);
         }
         l_run += ls;
-        // P V of block j-1 has read P and accumulated O
-        if (j > 0) {
+        if (__any_sync(0xffffffffu, resc)) {  // warp-collective TMEM access
+          // P V of block j-1 has accumulated into O (j > 0: no row has O yet at j = 0)
           ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (n - 1) & 1, a.status));
           if (!ok) break;
           tc_fence_after();
-        }
-        if (__any_sync(0xffffffffu, resc)) {  // warp-collective TMEM access
 #pragma unroll 1
           for (int c0 = 0; c0 < 128; c0 += 32) {
             uint32_t ov[32];
@@ -311,15 +317,19 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
           }
           tmem_st_wait();
         }
-        uint8_t* prow = sm + OFF_P + tid * 128;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          *reinterpret_cast<uint4*>(prow + ((cc ^ (tid & 7)) << 4)) =
-              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-        fence_async_smem();
+        // P_j over the columns of S_j (already read into registers)
+        tmem_st32x(tmem + lane_base + COL_S + bf * 64, pk);
+        tmem_st_wait();
+        // Consume P V of block j-1 before signalling P_j, so this warp takes
+        // bar_pv's phases in order: P V of block j-2 has completed (S_j was
+        // issued after it) and P V of block j cannot start before the signal.
+        if (j > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (n - 1) & 1, a.status));
+          if (!ok) break;
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_pfull);
+        if (lane == 0) mbar_arrive(&bar_pfull[bf]);
       }
       if (ok && nblk > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (seq0 + nblk - 1) & 1, a.status));
       if (!ok) {
@@ -397,7 +407,7 @@ extern "C" int msa_fwd(const msa_problem* p, const uint16_t* q, const uint16_t* 
     return MSA_ERR_CUDA;
   layout_kernel<<<1, 1024, 0, st>>>(p->cu_seqlens, p->kv_doc_starts, N, p->total_tokens, p->kv_rows,
                                     p->num_blocks, p->num_chunks, blk_off, chunk_off, d_status);
-  // The largest shared-memory carveout: two CTAs of ~113 KB share one SM.
+  // The largest shared-memory carveout: two CTAs of ~97 KB share one SM.
   if (cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fwd::SMEM) != cudaSuccess ||
       cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
