@@ -121,8 +121,10 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
   uint64_t* bar_k = bar_q + 2;      // two
   uint64_t* bar_v = bar_q + 4;      // two
   uint64_t* bar_s = bar_q + 6;      // two: S full (MMA commit)
-  // two: P written and O rescaled (4 softmax warps).  One per S/P buffer:
-  // block j+1's softmax may finish before the issuer has waited for block j's.
+  // two: P written and O rescaled (4 softmax warps), one per S/P buffer.
+  // Block j+1's softmax signals only after P V of block j, which itself
+  // follows the issuer's wait for block j, so one would do; two keep the
+  // issuer's wait independent of that ordering.
   uint64_t* bar_pfull = bar_q + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 11);
   int* s_blocks = reinterpret_cast<int*>(bar_q + 12);  // up to 32 selected blocks, count at [32]
