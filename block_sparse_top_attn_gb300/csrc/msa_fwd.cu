@@ -3,8 +3,8 @@
 // rows (8 tokens x 16 q-heads) attend the chunk's selected key blocks
 // causally, in one pass with an online softmax:
 //   S_j = Q K_j^T (tcgen05, fp32 in TMEM), m = running row max (log2 units),
-//   P_j = exp2(S_j - m) (bf16, in TMEM over the columns of S_j),
-//   l += rowsum(P_j), O += P_j V_j (TMEM, the GEMM reads P_j from TMEM).
+//   P_j = exp2(S_j - m) (bf16, in TMEM), l += rowsum(P_j),
+//   O += P_j V_j (TMEM; the GEMM reads P_j from TMEM).
 // The running max is moved only when a block raises it by more than kTau
 // (so P stays below 2^kTau); O is then rescaled in TMEM by exp2(m_old - m_new).
 // O = O / l is written as bf16 and LSE = (m + log2 l) ln 2, the form the
@@ -12,9 +12,10 @@
 //
 // Warps 0-3 run the softmax, one row per thread; warp 4 loads tiles (TMA) and
 // issues the GEMMs.  They hand off through mbarriers: S_j full (MMA commit),
-// P_j written (softmax), P_j V_j done (MMA commit).  S/P is double-buffered in
-// TMEM: S_{j+1} is computed while block j's softmax runs, once P_{j-1} V_{j-1}
-// has read the buffer.  K and V are double-buffered in smem and loaded ahead.
+// S_j read (softmax), P_j written (softmax), P_j V_j done (MMA commit).  TMEM
+// holds one S buffer, two P buffers and O: S_{j+1} is computed as soon as
+// block j's softmax has read S_j, while P_j V_j runs from the other P buffer.
+// K and V are double-buffered in smem and loaded ahead.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -39,11 +40,17 @@ constexpr uint32_t BAR_BYTES = 256;
 constexpr uint32_t ALIGN_SLACK = 768;
 constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + ALIGN_SLACK;
 constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t COL_S = 0, COL_O = 128;  // S/P buffers at 0 and 64 (P: first 32 columns)
+constexpr uint32_t COL_S = 0, COL_P = 64, COL_O = 128;  // S 64 columns, P 2 x 32 (bf16 pairs), O 128
 constexpr float kTau = 8.f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 }  // namespace fwd
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 __device__ __forceinline__ float lg2_approx(float x) {
   float y;
@@ -120,8 +127,9 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
   uint64_t* bar_pv = bar_q + 1;     // P V done (MMA commit)
   uint64_t* bar_k = bar_q + 2;      // two
   uint64_t* bar_v = bar_q + 4;      // two
-  uint64_t* bar_s = bar_q + 6;      // two: S full (MMA commit)
-  // two: P written and O rescaled (4 softmax warps), one per S/P buffer.
+  uint64_t* bar_s = bar_q + 6;      // S full (MMA commit)
+  uint64_t* bar_sfree = bar_q + 7;  // S read (4 softmax warps)
+  // two: P written and O rescaled (4 softmax warps), one per P buffer.
   // Block j+1's softmax signals only after P V of block j, which itself
   // follows the issuer's wait for block j, so one would do; two keep the
   // issuer's wait independent of that ordering.
@@ -132,10 +140,11 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
   if (tid == 0) {
     mbar_init(bar_q, 1);
     mbar_init(bar_pv, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_sfree, 4);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_k[i], 1);
       mbar_init(&bar_v[i], 1);
-      mbar_init(&bar_s[i], 1);
       mbar_init(&bar_pfull[i], 4);
     }
     fence_mbar_init();
@@ -152,8 +161,9 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
   const uint32_t sbase = smem_u32(sm);
   constexpr uint32_t ID_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t ID_O = idesc_bf16_f32(128, 128, false, true);
-  // Blocks processed so far by this CTA: block n uses K/V/S/P buffer n & 1 and
-  // phase parity (n >> 1) & 1 of their barriers, parity n & 1 of bar_pv.
+  // Blocks processed so far by this CTA: block n uses K/V/P buffer n & 1 and
+  // phase parity (n >> 1) & 1 of their barriers, parity n & 1 of bar_s,
+  // bar_sfree and bar_pv (one phase per block).
   uint32_t seq = 0, ph_q = 0;
   bool aborted = status_bad(a.status);
   const int64_t items = (int64_t)a.Hi * a.NC;
@@ -196,43 +206,39 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
-              umma_bf16(tmem + COL_S + (seq0 & 1) * 64, sdesc_sw128(sbase + OFF_Q + half * 16384 + sub, 16, 1024),
+              umma_bf16(tmem + COL_S, sdesc_sw128(sbase + OFF_Q + half * 16384 + sub, 16, 1024),
                         sdesc_sw128(sbase + OFF_K + (seq0 & 1) * 16384 + half * 8192 + sub, 16, 1024), ID_S,
                         kk > 0);
             }
-            umma_commit(&bar_s[seq0 & 1]);
+            umma_commit(bar_s);
           }
           __syncwarp();
         }
         for (int j = 0; j < nblk && ok; ++j) {
           const uint32_t n = seq0 + j, bf = n & 1;
-          // S_{j+1} once K_{j+1} has landed and P V of block j-1 has read the
-          // S/P buffer it goes into (block j-1's softmax wrote P before that)
+          // S_{j+1} once K_{j+1} has landed and every softmax warp has read S_j;
+          // then K_{j+2} into the K buffer S_j read (S_j completed before it was read)
           if (j + 1 < nblk) {
             const uint32_t n1 = n + 1, b1 = n1 & 1;
             ok = __all_sync(0xffffffffu, mbar_wait(&bar_k[b1], (n1 >> 1) & 1, a.status) &&
-                                             (j == 0 || mbar_wait(bar_pv, (n - 1) & 1, a.status)));
+                                             mbar_wait(bar_sfree, n & 1, a.status));
             if (!ok) break;
             tc_fence_after();
             if (elect_one()) {
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
-                umma_bf16(tmem + COL_S + b1 * 64, sdesc_sw128(sbase + OFF_Q + half * 16384 + sub, 16, 1024),
+                umma_bf16(tmem + COL_S, sdesc_sw128(sbase + OFF_Q + half * 16384 + sub, 16, 1024),
                           sdesc_sw128(sbase + OFF_K + b1 * 16384 + half * 8192 + sub, 16, 1024), ID_S, kk > 0);
               }
-              umma_commit(&bar_s[b1]);
+              umma_commit(bar_s);
+              if (j + 2 < nblk) load_kv(sm + OFF_K + bf * 16384, &tmK, &bar_k[bf], hi, kv0 + s_blocks[j + 2] * 64);
             }
             __syncwarp();
           }
-          // K_{j+2} into this K buffer once S_j (its reader) has completed
-          if (j + 2 < nblk) {
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[bf], (n >> 1) & 1, a.status)))) break;
-            if (elect_one()) load_kv(sm + OFF_K + bf * 16384, &tmK, &bar_k[bf], hi, kv0 + s_blocks[j + 2] * 64);
-            __syncwarp();
-          }
-          // V_{j+1} into the other V buffer (P V of block j-1 has completed: waited above)
+          // V_{j+1} into the V buffer P V of block j-1 read, once that has completed
           if (j >= 1 && j + 1 < nblk) {
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (n - 1) & 1, a.status)))) break;
             if (elect_one())
               load_kv(sm + OFF_V + (bf ^ 1) * 16384, &tmV, &bar_v[bf ^ 1], hi, kv0 + s_blocks[j + 1] * 64);
             __syncwarp();
@@ -246,7 +252,7 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
           if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_bf16_ts(tmem + COL_O, tmem + COL_S + bf * 64 + kk * 8,
+              umma_bf16_ts(tmem + COL_O, tmem + COL_P + bf * 32 + kk * 8,
                            sdesc_sw128(sbase + OFF_V + bf * 16384 + kk * 2048, 8192, 1024), ID_O,
                            (j > 0 || kk > 0) ? 1u : 0u);
             umma_commit(bar_pv);
@@ -268,41 +274,63 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
       for (int j = 0; j < nblk; ++j) {
         const uint32_t n = seq0 + j, bf = n & 1;
         const int b = s_blocks[j];
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[bf], (n >> 1) & 1, a.status));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_s, n & 1, a.status));
         if (!ok) break;
         tc_fence_after();
+        // raw scores; keys after the row's query masked to -inf.  A block that
+        // ends before the chunk's first query needs no mask: every key precedes
+        // every real row, and rows past the document end (their queries are
+        // real tokens or TMA zero fill, so finite) are never stored.
+        const bool full = b * 64 + 63 <= c * 8;
         float xs[64];
-        float bmax = -CUDART_INF_F;
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          uint32_t sv[32];
-          tmem_ld32x(tmem + lane_base + COL_S + bf * 64 + c0, sv);
+        {
+          uint32_t sv0[32], sv1[32];
+          tmem_ld32x(tmem + lane_base + COL_S, sv0);
+          tmem_ld32x(tmem + lane_base + COL_S + 32, sv1);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const bool valid = qpos >= 0 && b * 64 + c0 + e <= qpos;
-            const float x = valid ? __uint_as_float(sv[e]) * a.scale_log2 : -CUDART_INF_F;
-            xs[c0 + e] = x;
-            bmax = fmaxf(bmax, x);
+            xs[e] = __uint_as_float(sv0[e]);
+            xs[32 + e] = __uint_as_float(sv1[e]);
           }
         }
-        const bool upd = bmax > m_run + kTau;  // also true for the row's first key
+        if (!full) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (b * 64 + e > qpos) xs[e] = -CUDART_INF_F;
+        }
+        float m4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+        for (int e = 0; e < 64; e += 8) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) m4[r] = max3(m4[r], xs[e + 2 * r], xs[e + 2 * r + 1]);
+        }
+        const float smax = max3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+        // S_j is in registers: the next S GEMM may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sfree);
+        const float bmax = smax * a.scale_log2;  // log2 units (scale > 0)
+        const bool upd = bmax > m_run + kTau;    // also true for the row's first key
         const bool resc = upd && m_run > -CUDART_INF_F;
         const float alpha = upd ? ex2_approx(m_run - bmax) : 1.f;
         if (upd) {
           l_run *= alpha;
           m_run = bmax;
         }
+        // p = exp2(x scale - m); masked keys give exp2(-inf) = 0, and a row
+        // with no key yet (m = -inf) uses 0 for m so nothing is inf - inf
+        const float nm = m_run > -CUDART_INF_F ? -m_run : 0.f;
         uint32_t pk[32];
-        float ls = 0.f;
+        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
-          const float p0 = xs[e] > -CUDART_INF_F ? ex2_approx(xs[e] - m_run) : 0.f;
-          const float p1 = xs[e + 1] > -CUDART_INF_F ? ex2_approx(xs[e + 1] - m_run) : 0.f;
-          ls += p0 + p1;
+          const float p0 = ex2_approx(fmaf(xs[e], a.scale_log2, nm));
+          const float p1 = ex2_approx(fmaf(xs[e + 1], a.scale_log2, nm));
+          ls4[(e >> 1) & 3] += p0 + p1;
           pk[e >> 1] = pack_bf16x2(p0, p1);
         }
-        l_run += ls;
+        l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
         if (__any_sync(0xffffffffu, resc)) {  // warp-collective TMEM access
           // P V of block j-1 has accumulated into O (j > 0: no row has O yet at j = 0)
           ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (n - 1) & 1, a.status));
@@ -319,12 +347,13 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
           }
           tmem_st_wait();
         }
-        // P_j over the columns of S_j (already read into registers)
-        tmem_st32x(tmem + lane_base + COL_S + bf * 64, pk);
+        // P_j into P buffer bf, which P V of block j-2 read: this warp waited
+        // for that P V in block j-1, before it signalled P_{j-1}
+        tmem_st32x(tmem + lane_base + COL_P + bf * 32, pk);
         tmem_st_wait();
         // Consume P V of block j-1 before signalling P_j, so this warp takes
-        // bar_pv's phases in order: P V of block j-2 has completed (S_j was
-        // issued after it) and P V of block j cannot start before the signal.
+        // bar_pv's phases in order: P V of block j-2 was consumed in block j-1
+        // and P V of block j cannot start before the signal.
         if (j > 0) {
           ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (n - 1) & 1, a.status));
           if (!ok) break;

@@ -33,13 +33,16 @@ class _Bar:
 
 
 def _simulate(items, seed, n_softmax=2, split_pfull=True, in_order_pv=True):
+    """One S buffer, two P buffers and O in TMEM; K and V double-buffered."""
     rng = random.Random(seed)
-    B = {n: _Bar(n) for n in ["q", "pv", "k0", "k1", "v0", "v1", "s0", "s1"]}
+    B = {n: _Bar(n) for n in ["q", "pv", "s", "k0", "k1", "v0", "v1"]}
+    B["sfree"] = _Bar("sfree", n_softmax)
     pf = ["pf0", "pf1"] if split_pfull else ["pf", "pf"]
     for n in set(pf):
         B[n] = _Bar(n, n_softmax)
     mma_q, tma = [], []
-    smK, smV, tmS = {0: None, 1: None}, {0: None, 1: None}, {0: None, 1: None}
+    smK, smV, tmP = {0: None, 1: None}, {0: None, 1: None}, {0: None, 1: None}
+    tmS = [None]
     done_S, done_PV = set(), set()
 
     def pf_phase(n):
@@ -64,18 +67,17 @@ def _simulate(items, seed, n_softmax=2, split_pfull=True, in_order_pv=True):
                 mma_q.append(("S", seq0))
                 for j in range(nblk):
                     n, bf = seq0 + j, (seq0 + j) & 1
-                    if j + 1 < nblk:          # S_{j+1}: K landed, P_{j-1} V_{j-1} done
+                    if j + 1 < nblk:          # S_{j+1}: K landed, every warp has read S_j
                         while not B[f"k{(n + 1) & 1}"].ready((n + 1) >> 1):
                             yield None
-                        if j >= 1:
-                            while not B["pv"].ready(n - 1):
-                                yield None
-                        mma_q.append(("S", n + 1))
-                    if j + 2 < nblk:          # K_{j+2} once S_j has completed
-                        while not B[f"s{bf}"].ready(n >> 1):
+                        while not B["sfree"].ready(n):
                             yield None
-                        tma.append((f"k{bf}", bf, "K", n + 2))
-                    if j >= 1 and j + 1 < nblk:   # V_{j+1} (P V of block j-1 waited above)
+                        mma_q.append(("S", n + 1))
+                        if j + 2 < nblk:      # K_{j+2} where K_j was (S_j done)
+                            tma.append((f"k{bf}", bf, "K", n + 2))
+                    if j >= 1 and j + 1 < nblk:   # V_{j+1} once P V of block j-1 is done
+                        while not B["pv"].ready(n - 1):
+                            yield None
                         tma.append((f"v{bf ^ 1}", bf ^ 1, "V", n + 1))
                     while not B[pf[bf]].ready(pf_phase(n)):
                         yield None
@@ -92,15 +94,18 @@ def _simulate(items, seed, n_softmax=2, split_pfull=True, in_order_pv=True):
             yield "sync"
             for j in range(nblk):
                 n, bf = seq0 + j, (seq0 + j) & 1
-                while not B[f"s{bf}"].ready(n >> 1):
+                while not B["s"].ready(n):
                     yield None
-                assert tmS[bf] in (("S", n), ("P", n))
+                assert tmS[0] == n, "S_j overwritten before it was read"
+                yield None
+                B["sfree"].arrive()
                 yield None
                 if j > 0 and rng.random() < 0.3:      # O rescale
                     while not B["pv"].ready(n - 1):
                         yield None
                     assert (n - 1) in done_PV and n not in done_PV
-                tmS[bf] = ("P", n)
+                assert n < 2 or (n - 2) in done_PV, "P stored over a P not yet read"
+                tmP[bf] = n
                 if j > 0 and in_order_pv:
                     while not B["pv"].ready(n - 1):
                         yield None
@@ -118,12 +123,12 @@ def _simulate(items, seed, n_softmax=2, split_pfull=True, in_order_pv=True):
             kind, n = mma_q.pop(0)
             if kind == "S":
                 assert smK[n & 1] == n, "S before its K landed"
-                assert n < 2 or (n - 2) in done_PV, "S over a P not yet read"
-                tmS[n & 1] = ("S", n)
+                assert B["sfree"].done >= n, "S over an S not yet read"
+                tmS[0] = n
                 done_S.add(n)
-                B[f"s{n & 1}"].arrive()
+                B["s"].arrive()
             else:
-                assert tmS[n & 1] == ("P", n), "P V before P was written"
+                assert tmP[n & 1] == n, "P V before P was written"
                 assert smV[n & 1] == n, "P V before its V landed"
                 done_PV.add(n)
                 B["pv"].arrive()
