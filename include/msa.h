@@ -216,12 +216,20 @@ int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uint16_t* k, c
                    void* ws, size_t ws_bytes, void* stream, uint32_t stages);
 
 /* The forward pass that produces O and LSE from the same selection
- * ("msa_bindings" page, sparse_atten_func, the flat forward).
+ * ("msa_bindings" page, sparse_atten_func, the flat forward): for each query
+ * row, softmax(scale * q k^T) over the keys of its chunk's selected blocks
+ * that precede or equal it, times V.  One pass with an online softmax; P is
+ * rounded to bf16 for the P V product, everything else accumulates in fp32.
+ * q     device bf16 [T, Hq, 128];  k, v device bf16 [W, Hkv, 128].
  * sel   device int32 [Hi, NC, K], as for msa_build_k2q (validated there,
  *       not here: call the forward with a selection the CSR build accepted).
  * o     device bf16 [T, Hq, 128] out;  lse device fp32 [T, Hq] out (natural
  *       log; -inf for a query that attends no key, whose O is 0).
- * ws    workspace of at least msa_workspace_bytes() bytes.
+ * ws    device workspace of at least 8 * (num_docs + 1) bytes rounded up to
+ *       256 (msa_workspace_bytes() is always enough); caller-owned.
+ * Returns MSA_ERR_INVALID_ARGUMENT for a null or misaligned pointer or a short
+ * ws, MSA_ERR_CUDA if a launch fails; a device wait that exceeds its bound
+ * writes MSA_ERR_TIMEOUT to *d_status.  Asynchronous on stream.
  */
 int msa_fwd(const msa_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,
             const int32_t* sel, uint16_t* o, float* lse, int32_t* d_status, void* ws,
