@@ -63,3 +63,12 @@ def test_ranks_draw_independent_batches():
     b = W.make_problem("tiny", seed=1, values=False)
     assert a.sel.shape == b.sel.shape
     assert not np.array_equal(a.sel, b.sel)
+
+
+def test_traffic_record_applies_only_to_its_workload_and_tiling():
+    sys.path.insert(0, ROOT)
+    import bench
+    rec = bench._traffic_record("long128k", 1024)
+    assert rec is None or rec > 0          # None once the kernel sources changed since the capture
+    assert bench._traffic_record("single8k", 0) is None
+    assert bench._traffic_record("long128k", 512) is None
