@@ -78,3 +78,63 @@ def test_forward_edge_cases(B, case):
     assert np.array_equal(empty, ~np.isfinite(gl))          # exactly the rows with no key
     assert np.all(from_bf16_tensor(o)[empty] == 0)
     assert np.max(np.abs(gl[~empty] - rl[~empty])) < 2e-3
+
+
+def _forward_parity(B, pb):
+    import torch
+    prob, t = upload(pb)
+    o, lse, st = B.forward(prob, t["sel"], t["q"], t["k"], t["v"])
+    torch.cuda.synchronize()
+    assert int(st[0].item()) == 0
+    ro, rl = O.forward_blocked(pb.q, pb.k, pb.v, pb.cu_seqlens, pb.kv_doc_starts, pb.sel, pb.block, pb.chunk,
+                               pb.softmax_scale)
+    assert_grad_close("o", from_bf16_tensor(o), ro)
+    gl = lse.cpu().numpy().astype(np.float64)
+    assert np.array_equal(~np.isfinite(rl), ~np.isfinite(gl))
+    fin = np.isfinite(rl)
+    assert np.max(np.abs(gl[fin] - rl[fin])) < 2e-3
+
+
+def test_forward_many_documents(B):
+    """Sixty documents of 1..599 tokens with K/V rows at aligned, gapped
+    offsets: every item looks its document up among many and reads its keys
+    at a document-local block offset."""
+    rng = np.random.default_rng(21)
+    lengths = [int(x) for x in rng.integers(1, 600, size=60)]
+    pb = W.make_problem(lengths=lengths, num_index_heads=2, topk=6, policy="diag_uniform", kv_layout="aligned",
+                        seed=21)
+    _forward_parity(B, pb)
+
+
+@pytest.mark.parametrize("name", ["varlen32k", "zipf64k"])
+def test_forward_large_sampled(B, name):
+    """The mid-size workloads at full size: 300 random (index head, document,
+    chunk) items, each checked against the oracle's per-chunk forward."""
+    import torch
+    pb = W.make_problem(name)
+    prob, t = upload(pb)
+    o, lse, st = B.forward(prob, t["sel"], t["q"], t["k"], t["v"])
+    torch.cuda.synchronize()
+    assert int(st[0].item()) == 0
+    go = from_bf16_tensor(o)
+    gl = lse.cpu().numpy().astype(np.float64)
+    lay = O.DocLayout(pb.cu_seqlens, pb.block, pb.chunk)
+    G = pb.num_q_heads // pb.sel.shape[0]
+    rng = np.random.default_rng(5)
+    got_o, ref_o, got_l, ref_l = [], [], [], []
+    for _ in range(300):
+        hi = int(rng.integers(pb.sel.shape[0]))
+        d = int(rng.integers(lay.num_docs))
+        c = int(rng.integers(int(lay.nc[d])))
+        qp, oc, lc = O.chunk_forward(pb.q, pb.k, pb.v, lay, pb.kv_doc_starts, pb.sel, hi, d, c, G,
+                                     pb.softmax_scale)
+        rows = int(lay.cu[d]) + qp
+        got_o.append(go[rows, hi * G:(hi + 1) * G])
+        ref_o.append(oc.transpose(1, 0, 2))
+        got_l.append(gl[rows, hi * G:(hi + 1) * G])
+        ref_l.append(lc.T)
+    assert_grad_close("o", np.concatenate(got_o), np.concatenate(ref_o))
+    gl_s, rl_s = np.concatenate(got_l), np.concatenate(ref_l)
+    assert np.array_equal(np.isfinite(gl_s), np.isfinite(rl_s))
+    fin = np.isfinite(rl_s)
+    assert np.max(np.abs(gl_s[fin] - rl_s[fin])) < 2e-3
