@@ -52,6 +52,27 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return r;
 }
 
+// Two fp32 lanes in one 64-bit register, for the paired fp32 FMA/add of sm_100+
+// (each lane rounds exactly as the scalar instruction).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 __device__ __forceinline__ float lg2_approx(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -322,15 +343,22 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
         // with no key yet (m = -inf) uses 0 for m so nothing is inf - inf
         const float nm = m_run > -CUDART_INF_F ? -m_run : 0.f;
         uint32_t pk[32];
-        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nm2 = f2_pack(nm, nm);
+        uint64_t ls2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
-          const float p0 = ex2_approx(fmaf(xs[e], a.scale_log2, nm));
-          const float p1 = ex2_approx(fmaf(xs[e + 1], a.scale_log2, nm));
-          ls4[(e >> 1) & 3] += p0 + p1;
+          float y0, y1;
+          f2_unpack(f2_fma(f2_pack(xs[e], xs[e + 1]), sc2, nm2), y0, y1);
+          const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+          ls2[(e >> 1) & 1] = f2_add(ls2[(e >> 1) & 1], f2_pack(p0, p1));
           pk[e >> 1] = pack_bf16x2(p0, p1);
         }
-        l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(ls2[0], a0, a1);
+          f2_unpack(ls2[1], b0, b1);
+          l_run += (a0 + a1) + (b0 + b1);
+        }
         if (__any_sync(0xffffffffu, resc)) {  // warp-collective TMEM access
           // P V of block j-1 has accumulated into O (j > 0: no row has O yet at j = 0)
           ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (n - 1) & 1, a.status));
