@@ -1,0 +1,287 @@
+"""CPU model check of the backward main kernel's hand-off protocol (no GPU).
+
+`msa_bwd_ws.cuh` runs, per CTA, an info warp, a TMA producer, two MMA issuers,
+softmax warps and reduce warps.  They hand off through mbarriers waited by
+phase parity:
+* an 8-entry task-info ring, released by the reduce warps;
+* K/V per bucket segment;
+* a two-stage Q/dO ring;
+* S/dP in TMEM;
+* P/dS in shared memory;
+* dQ double-buffered in TMEM;
+* dK/dV in TMEM per segment.
+
+This model replays each role's order of waits, arrivals, loads and GEMM
+groups under random interleavings.  Each issuer's GEMMs complete in its own
+issue order, and the two issuers complete in any relative order.  Two softmax
+warps stand in for sixteen and two reduce warps for four.  The model asserts
+that every parity wait sees the awaited or just-completed phase.  It asserts
+that no buffer (info entry, K/V, Q/dO stage, S/dP, P/dS, dQ, dK/dV) is
+rewritten before its last reader is done, and that every reader sees the
+task's own data.
+"""
+import random
+
+import pytest
+
+N_SOFT, N_RED, K_INFO = 2, 2, 8
+
+
+class _Bar:
+    def __init__(self, name, count=1):
+        self.name, self.done, self.count, self.arr = name, 0, count, 0
+
+    def arrive(self):
+        self.arr += 1
+        if self.arr == self.count:
+            self.arr, self.done = 0, self.done + 1
+
+    def ready_parity(self, parity, k):
+        """Wait by parity for the k-th completion (0-based); k = -1 is the
+        phase before the first, complete from the start."""
+        assert self.done in (k, k + 1), f"parity alias on {self.name}: phase {k}, completed {self.done}"
+        assert parity == (k & 1) or k < 0
+        return self.done >= k + 1
+
+
+def _segments(rng, n_tasks):
+    seg, out, left = 0, [], 0
+    for j in range(n_tasks):
+        if left == 0:
+            left = rng.randint(1, 5)
+            first = True
+        else:
+            first = False
+        left -= 1
+        last = left == 0 or j == n_tasks - 1
+        out.append((seg, first, last))
+        if last:
+            seg += 1
+            left = 0
+    return out
+
+
+def _simulate(n_tasks, seed, swap_release=False):
+    rng = random.Random(seed)
+    tasks = _segments(rng, n_tasks)
+    B = {}
+    for n in ["kv", "k_empty", "v_empty", "s_full", "dkv_full"] + [f"q_full{i}" for i in range(2)] + \
+             [f"do_full{i}" for i in range(2)] + [f"q_empty{i}" for i in range(2)] + \
+             [f"do_empty{i}" for i in range(2)] + ["pds_empty"] + [f"dq_full{i}" for i in range(2)]:
+        B[n] = _Bar(n)
+    B["s_empty"] = _Bar("s_empty", N_SOFT)
+    B["pds_full"] = _Bar("pds_full", N_SOFT)
+    for i in range(2):
+        B[f"dq_empty{i}"] = _Bar(f"dq_empty{i}", N_RED)
+    B["dkv_empty"] = _Bar("dkv_empty", N_RED)
+    for i in range(K_INFO):
+        B[f"info_full{i}"] = _Bar(f"info_full{i}")
+        B[f"info_empty{i}"] = _Bar(f"info_empty{i}", N_RED)
+
+    info = [None] * K_INFO            # task index held by each ring entry
+    read_info = {}                    # role -> highest task whose info it has read
+    smQ, smDO = [None, None], [None, None]
+    smKV = [None]                     # segment held by K/V
+    tmSdP = [None]                    # task whose S/dP is in TMEM
+    smPdS = [None]
+    tmDQ = [None, None]
+    tmDKV = [None]                    # segment whose dK/dV accumulate in TMEM
+    doneA, doneB = set(), set()       # completed GEMM groups (S/dP; dV/dK/dQ)
+    sdp_read, pds_written = {}, {}    # task -> softmax warps done reading S/dP / writing P/dS
+    dq_read, dkv_read = {}, {}        # task / segment -> reduce warps done
+    qA, qB, tma = [], [], []
+
+    def note_read(role, j):
+        read_info[role] = max(read_info.get(role, -1), j)
+
+    def info_warp():
+        for j in range(n_tasks + 1):          # + the sentinel
+            slot = j % K_INFO
+            k = j // K_INFO - 1                # phase of INFO_EMPTY released by task j-8
+            while not B[f"info_empty{slot}"].ready_parity(((j // K_INFO) & 1) ^ 1, k):
+                yield
+            if j >= K_INFO:
+                assert all(read_info.get(r, -1) >= j - K_INFO for r in
+                           ["load", "A", "B"] + [f"soft{w}" for w in range(N_SOFT)] +
+                           [f"red{w}" for w in range(N_RED)]), "info entry rewritten before every role read it"
+            info[slot] = j
+            B[f"info_full{slot}"].arrive()
+            yield
+
+    def get_info(role, j):
+        slot = j % K_INFO
+        while not B[f"info_full{slot}"].ready_parity((j // K_INFO) & 1, j // K_INFO):
+            yield
+        assert info[slot] == j, "info entry overwritten"
+        note_read(role, j)
+
+    def producer():
+        for j in range(n_tasks):
+            yield from get_info("load", j)
+            seg, first, last = tasks[j]
+            if first:
+                while not B["k_empty"].ready_parity((seg & 1) ^ 1, seg - 1):
+                    yield
+                while not B["v_empty"].ready_parity((seg & 1) ^ 1, seg - 1):
+                    yield
+                tma.append(("kv", seg))
+            st, k = j & 1, (j >> 1) - 1
+            while not B[f"q_empty{st}"].ready_parity(((j >> 1) & 1) ^ 1, k):
+                yield
+            tma.append(("q", j))
+            while not B[f"do_empty{st}"].ready_parity(((j >> 1) & 1) ^ 1, k):
+                yield
+            tma.append(("do", j))
+        yield from get_info("load", n_tasks)
+
+    def issuer_a():
+        for j in range(n_tasks):
+            yield from get_info("A", j)
+            seg, first, last = tasks[j]
+            st = j & 1
+            if first:
+                while not B["kv"].ready_parity(seg & 1, seg):
+                    yield
+            while not B["s_empty"].ready_parity((j & 1) ^ 1, j - 1):
+                yield
+            while not B[f"q_full{st}"].ready_parity((j >> 1) & 1, j >> 1):
+                yield
+            while not B[f"do_full{st}"].ready_parity((j >> 1) & 1, j >> 1):
+                yield
+            qA.append(("SdP", j))
+        yield from get_info("A", n_tasks)
+
+    def issuer_b():
+        for j in range(n_tasks):
+            yield from get_info("B", j)
+            seg, first, last = tasks[j]
+            st = j & 1
+            while not B["pds_full"].ready_parity(j & 1, j):
+                yield
+            if first:
+                while not B["dkv_empty"].ready_parity((seg & 1) ^ 1, seg - 1):
+                    yield
+            while not B[f"dq_empty{st}"].ready_parity(((j >> 1) & 1) ^ 1, (j >> 1) - 1):
+                yield
+            qB.append(("dVdKdQ", j))
+        yield from get_info("B", n_tasks)
+
+    def softmax(w):
+        role = f"soft{w}"
+        yield from get_info(role, 0)
+        for j in range(n_tasks):
+            yield from get_info(role, j + 1)          # look-ahead: the next task's row scalars
+            while not B["s_full"].ready_parity(j & 1, j):
+                yield
+            assert tmSdP[0] == j, "S/dP read before it was computed or after it was overwritten"
+            yield
+            sdp_read[j] = sdp_read.get(j, 0) + 1
+            B["s_empty"].arrive()
+            while not B["pds_empty"].ready_parity((j & 1) ^ 1, j - 1):
+                yield
+            assert j == 0 or (j - 1) in doneB, "P/dS stored over the previous task's before its GEMMs ran"
+            smPdS[0] = j
+            pds_written[j] = pds_written.get(j, 0) + 1
+            B["pds_full"].arrive()
+            yield
+
+    def reducer(w):
+        role = f"red{w}"
+        for j in range(n_tasks):
+            yield from get_info(role, j)
+            seg, first, last = tasks[j]
+            pb = j & 1
+            while not B[f"dq_full{pb}"].ready_parity((j >> 1) & 1, j >> 1):
+                yield
+            assert tmDQ[pb] == j, "dQ read before it was computed or after it was overwritten"
+            yield
+            dq_read[j] = dq_read.get(j, 0) + 1
+            B[f"dq_empty{pb}"].arrive()
+            if last:
+                while not B["dkv_full"].ready_parity(seg & 1, seg):
+                    yield
+                assert tmDKV[0] == seg and (j in doneB), "dK/dV read before the segment finished"
+                yield
+                dkv_read[seg] = dkv_read.get(seg, 0) + 1
+                B["dkv_empty"].arrive()
+            yield
+            B[f"info_empty{j % K_INFO}"].arrive()
+        yield from get_info(role, n_tasks)
+
+    def run_a():
+        if qA and rng.random() < 0.3:
+            _, j = qA.pop(0)
+            seg, first, last = tasks[j]
+            assert smQ[j & 1] == j and smDO[j & 1] == j, "S/dP before its Q/dO landed"
+            assert smKV[0] == seg, "S/dP before its K/V landed"
+            assert j == 0 or sdp_read.get(j - 1, 0) == N_SOFT, "S/dP over an S/dP not yet read"
+            tmSdP[0] = j
+            doneA.add(j)
+            B["s_full"].arrive()
+            if last:
+                B["v_empty"].arrive()
+
+    def run_b():
+        if qB and rng.random() < 0.3:
+            _, j = qB.pop(0)
+            seg, first, last = tasks[j]
+            assert smPdS[0] == j and pds_written.get(j, 0) == N_SOFT, "dV/dK/dQ before P/dS were stored"
+            assert smQ[j & 1] == j and smDO[j & 1] == j, "dV/dK/dQ after the Q/dO stage was reloaded"
+            assert smKV[0] == seg, "dQ after K was reloaded"
+            assert j < 2 or dq_read.get(j - 2, 0) == N_RED, "dQ over a buffer not yet drained"
+            if first:
+                assert seg == 0 or dkv_read.get(seg - 1, 0) == N_RED, "dK/dV overwritten before drained"
+                tmDKV[0] = seg
+            tmDQ[j & 1] = j
+            doneB.add(j)
+            for n in (["pds_empty", f"do_empty{j & 1}", f"q_empty{j & 1}"] if swap_release else
+                      ["pds_empty", f"q_empty{j & 1}", f"do_empty{j & 1}"]):
+                B[n].arrive()
+            B[f"dq_full{j & 1}"].arrive()
+            if last:
+                B["k_empty"].arrive()
+                B["dkv_full"].arrive()
+
+    def run_tma():
+        if tma and rng.random() < 0.3:
+            kind, x = tma.pop(rng.randrange(len(tma)))
+            if kind == "kv":
+                prev = [t for t in range(n_tasks) if tasks[t][0] == x - 1]
+                assert all(t in doneA and t in doneB for t in prev), "K/V reloaded before the segment's GEMMs ran"
+                smKV[0] = x
+                B["kv"].arrive()
+            elif kind == "q":
+                assert x < 2 or ((x - 2) in doneA and (x - 2) in doneB), "Q stage reloaded too early"
+                smQ[x & 1] = x
+                B[f"q_full{x & 1}"].arrive()
+            else:
+                assert x < 2 or ((x - 2) in doneA and (x - 2) in doneB), "dO stage reloaded too early"
+                smDO[x & 1] = x
+                B[f"do_full{x & 1}"].arrive()
+
+    roles = [info_warp(), producer(), issuer_a(), issuer_b()] + [softmax(w) for w in range(N_SOFT)] + \
+            [reducer(w) for w in range(N_RED)]
+    alive = list(range(len(roles)))
+    for _ in range(4 * 10 ** 5):
+        if not alive:
+            assert not qA and not qB and not tma
+            assert len(doneA) == len(doneB) == n_tasks, "a task's GEMMs never ran"
+            return
+        c = rng.random()
+        if c < 0.6:
+            i = rng.choice(alive)
+            try:
+                next(roles[i])
+            except StopIteration:
+                alive.remove(i)
+        else:
+            run_a()
+            run_b()
+            run_tma()
+    raise AssertionError("deadlock")
+
+
+def test_backward_protocol_holds_under_random_schedules():
+    rng = random.Random(0)
+    for seed in range(400):
+        _simulate(rng.randint(1, 24), seed)
