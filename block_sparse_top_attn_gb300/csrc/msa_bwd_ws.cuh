@@ -437,13 +437,18 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           const int lim = qpos - kbase;  // keys kbase + e with e <= lim are attended
           if (lim >= 15) {
             // the whole 16-key slice is attended (every block but the diagonal one)
+            // paired fp32 FMA/multiply: each lane rounds as the scalar form would
+            const uint64_t sl2 = f2_pack(a.scale_log2, a.scale_log2), nl2 = f2_pack(-lse2, -lse2);
+            const uint64_t sc2 = f2_pack(a.scale, a.scale), nd2 = f2_pack(-dsc, -dsc);
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {
-              const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), a.scale_log2, -lse2));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), a.scale_log2, -lse2));
+              float y0, y1, d0, d1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2, nl2), y0, y1);
+              const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+              const uint64_t t = f2_fma(f2_pack(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])), sc2, nd2);
+              f2_unpack(f2_mul(f2_pack(p0, p1), t), d0, d1);
               pk[e >> 1] = pack_bf16x2(p0, p1);
-              dk[e >> 1] = pack_bf16x2(p0 * fmaf(__uint_as_float(dpv[e]), a.scale, -dsc),
-                                       p1 * fmaf(__uint_as_float(dpv[e + 1]), a.scale, -dsc));
+              dk[e >> 1] = pack_bf16x2(d0, d1);
             }
           } else {
 #pragma unroll
