@@ -81,3 +81,28 @@ def test_invalid_arguments_rejected_on_host(B):
     p.num_q_heads = 16
     p.cu_seqlens = 4100  # misaligned
     assert lib.msa_workspace_bytes(ctypes.byref(p), 64, 8, 0) == 0
+
+
+def test_forward_arguments_rejected_on_host(B):
+    """msa_fwd rejects a null problem, null or misaligned buffers and a short
+    workspace before it touches the device (fake, never dereferenced addresses)."""
+    lib = B.lib
+    assert lib.msa_fwd(None, *([None] * 8), 0, None) == B.MSA_ERR_INVALID_ARGUMENT
+    p = B.msa_problem()
+    p.num_docs, p.total_tokens, p.kv_rows = 1, 64, 64
+    p.cu_seqlens, p.kv_doc_starts = 4096, 8192
+    p.num_q_heads, p.num_index_heads, p.num_kv_heads = 16, 1, 1
+    p.head_dim, p.block_size, p.query_chunk, p.topk = 128, 64, 8, 4
+    p.num_blocks, p.num_chunks, p.softmax_scale = 1, 8, 0.1
+    bufs = [1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20, 6 << 20, 7 << 20, 8 << 20]  # q k v sel o lse status ws
+    ws_ok = 256
+    for i in range(len(bufs)):
+        nulled = list(bufs)
+        nulled[i] = None
+        assert lib.msa_fwd(ctypes.byref(p), *nulled, ws_ok, None) == B.MSA_ERR_INVALID_ARGUMENT, i
+        shifted = list(bufs)
+        shifted[i] += 4
+        assert lib.msa_fwd(ctypes.byref(p), *shifted, ws_ok, None) == B.MSA_ERR_INVALID_ARGUMENT, i
+    assert lib.msa_fwd(ctypes.byref(p), *bufs, 8, None) == B.MSA_ERR_INVALID_ARGUMENT   # ws < 8 (N + 1), rounded
+    p.head_dim = 64
+    assert lib.msa_fwd(ctypes.byref(p), *bufs, ws_ok, None) == B.MSA_ERR_UNSUPPORTED_SHAPE
