@@ -138,3 +138,51 @@ def test_forward_large_sampled(B, name):
     assert np.array_equal(np.isfinite(gl_s), np.isfinite(rl_s))
     fin = np.isfinite(rl_s)
     assert np.max(np.abs(gl_s[fin] - rl_s[fin])) < 2e-3
+
+
+def _rows_with_rescale(pb, lay, chunks):
+    """Rows of the given (hi, d, c) chunks whose running max, taken over the
+    selected blocks in slot order, rises by more than 8 (log2 units) after
+    the row's first key: the kernel rescales O in TMEM for those."""
+    qf, kf = O.bf16_to_f64(pb.q), O.bf16_to_f64(pb.k)
+    G = pb.num_q_heads // pb.sel.shape[0]
+    n = 0
+    for hi, d, c in chunks:
+        t0, k0 = int(lay.cu[d]), int(pb.kv_doc_starts[d])
+        qp = lay.chunk_positions(d, c)
+        m = np.full((qp.size, G), -np.inf)
+        hit = np.zeros((qp.size, G), dtype=bool)
+        for b in (int(x) for x in pb.sel[hi, int(lay.chunk_off[d]) + c] if x >= 0):
+            keys = np.arange(b * 64, min(b * 64 + 64, int(lay.lengths[d])))
+            s = np.einsum("qhd,kd->qhk", qf[t0 + qp, hi * G:(hi + 1) * G], kf[k0 + keys, hi])
+            s = np.where(keys[None, None, :] <= qp[:, None, None], s * pb.softmax_scale / np.log(2.0), -np.inf)
+            bm = s.max(axis=2)
+            up = bm > m + 8
+            hit |= up & (m > -np.inf)
+            m = np.where(up, bm, m)
+        n += int(hit.sum())
+    return n
+
+
+def test_forward_rescales_o_when_the_max_jumps(B):
+    """K of about a third of the key blocks scaled by 8 (exact in bf16) and
+    block order shuffled: most rows meet a block that raises their running
+    max by more than 2^8, so the kernel's O rescale in TMEM runs."""
+    rng = np.random.default_rng(31)
+    pb = W.make_problem(lengths=[2048, 700], num_index_heads=2, topk=8, policy="diag_uniform", seed=31)
+    kf = O.bf16_to_f64(pb.k)
+    lay = O.DocLayout(pb.cu_seqlens, pb.block, pb.chunk)
+    for d in range(lay.num_docs):
+        k0 = int(pb.kv_doc_starts[d])
+        for b in range(int(lay.nb[d])):
+            if rng.random() < 0.35:
+                kf[k0 + b * 64:k0 + b * 64 + 64] *= 8.0
+    pb.k = O.f64_to_bf16(kf)
+    sel = pb.sel.copy()
+    for hi in range(sel.shape[0]):
+        for g in range(sel.shape[1]):
+            sel[hi, g] = sel[hi, g][rng.permutation(sel.shape[2])]
+    pb.sel = sel
+    sample = [(int(rng.integers(2)), d, int(rng.integers(int(lay.nc[d])))) for d in (0, 1) for _ in range(20)]
+    assert _rows_with_rescale(pb, lay, sample) > 0
+    _forward_parity(B, pb)
