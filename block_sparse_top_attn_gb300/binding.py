@@ -82,6 +82,7 @@ def _load():
         "msa_device_capability": (ctypes.c_int, [i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
         "msa_device_sm_count": (ctypes.c_int, [i32, ctypes.POINTER(i32)]),
         "msa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "msa_selftest_wait_timeout": (ctypes.c_int, [vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -91,6 +92,12 @@ def _load():
 
 
 lib = _load()
+
+
+def msa_selftest_wait_timeout(d_status, stream=None):
+    """Run the bounded-wait self-test kernel: *d_status becomes MSA_ERR_TIMEOUT
+    about two seconds later, with no fault and the context still usable."""
+    _check(lib.msa_selftest_wait_timeout(_ptr(d_status), _stream(stream)), "msa_selftest_wait_timeout")
 
 
 def status_string(code: int) -> str:

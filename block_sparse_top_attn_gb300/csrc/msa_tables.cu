@@ -718,3 +718,28 @@ int msa_build_tasks(const msa_problem* p, const int32_t* row_ptr, const int32_t*
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded waits: an mbarrier phase that nothing completes.
+// ---------------------------------------------------------------------------
+namespace msa {
+__global__ void selftest_wait_kernel(int32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // no thread ever arrives: the wait gives up after kWaitLimitNs and records
+  // MSA_ERR_TIMEOUT in *status
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, status);
+}
+}  // namespace msa
+
+extern "C" int msa_selftest_wait_timeout(int32_t* d_status, void* stream) {
+  if (!d_status || !msa::aligned16(d_status)) return MSA_ERR_INVALID_ARGUMENT;
+  int rc = msa::check_device_current();
+  if (rc) return rc;
+  msa::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(d_status);
+  return msa::cuda_status(cudaGetLastError());
+}

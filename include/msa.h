@@ -235,6 +235,16 @@ int msa_fwd(const msa_problem* p, const uint16_t* q, const uint16_t* k, const ui
             const int32_t* sel, uint16_t* o, float* lse, int32_t* d_status, void* ws,
             size_t ws_bytes, void* stream);
 
+/* Self-test of the bounded device waits (no counterpart in the pages).
+ * Launches one small kernel that waits, with the same bounded mbarrier wait
+ * every kernel of this library uses, for an mbarrier phase that nothing
+ * completes.  After the wait limit (2 s) the kernel writes MSA_ERR_TIMEOUT to
+ * *d_status (first error wins) and returns normally: no fault, no hang, and
+ * the CUDA context stays usable.  d_status: device int32, caller-owned.
+ * Returns MSA_ERR_INVALID_ARGUMENT for a null or misaligned d_status,
+ * MSA_ERR_CUDA if the launch fails.  Asynchronous on stream. */
+int msa_selftest_wait_timeout(int32_t* d_status, void* stream);
+
 /* Host-side walk rule ("msa_schedule" page): rows_per_cta, chunk_map and
  * grid_launch_bound.  chunk_map writes (full, tail, grid) to out3. */
 int32_t msa_rows_per_cta(int64_t num_rows);

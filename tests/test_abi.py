@@ -106,3 +106,8 @@ def test_forward_arguments_rejected_on_host(B):
     assert lib.msa_fwd(ctypes.byref(p), *bufs, 8, None) == B.MSA_ERR_INVALID_ARGUMENT   # ws < 8 (N + 1), rounded
     p.head_dim = 64
     assert lib.msa_fwd(ctypes.byref(p), *bufs, ws_ok, None) == B.MSA_ERR_UNSUPPORTED_SHAPE
+
+
+def test_selftest_wait_rejects_bad_status_pointer_on_host(B):
+    assert B.lib.msa_selftest_wait_timeout(None, None) == B.MSA_ERR_INVALID_ARGUMENT
+    assert B.lib.msa_selftest_wait_timeout(4100, None) == B.MSA_ERR_INVALID_ARGUMENT
