@@ -263,3 +263,40 @@ def test_bf16_rounding_of_float64_between_neighbours():
     assert O.f64_to_bf16(np.array([mid - 2.0 ** -40]))[0] == 0x3F80
     assert O.f64_to_bf16(np.array([mid + 2.0 ** -40]))[0] == 0x3F81
     assert O.f64_to_bf16(np.array([mid]))[0] == 0x3F80          # tie -> even
+
+
+def test_empty_chunk_attends_nothing():
+    """A chunk whose selection holds only -1 attends no key: its rows get O = 0
+    and LSE = -inf (dense and blocked forms alike), dQ = 0, and dK/dV do not
+    depend on those rows' dO."""
+    p = _problem(11, [70, 45], Hi=2, G=2, D=8, K=3, B=8, C=4)
+    sel = p["sel"].copy()
+    empty = [(0, 2), (1, 5), (0, 19), (1, 19)]            # (index head, global chunk)
+    for hi, g in empty:
+        sel[hi, g] = -1
+    p["sel"] = sel
+    lay = O.DocLayout(p["cu"], p["B"], p["C"])
+    G = 2
+    rows = {}
+    for hi, g in empty:
+        d = int(np.searchsorted(lay.chunk_off, g, side="right") - 1)
+        c = g - int(lay.chunk_off[d])
+        rows[(hi, g)] = int(lay.cu[d]) + lay.chunk_positions(d, c)
+    for fwd in (O.forward_dense, O.forward_blocked):
+        # the dense form evaluates exp(-inf - -inf) in a branch its mask discards
+        with np.errstate(invalid="ignore"):
+            o, lse = fwd(p["q"], p["k"], p["v"], p["cu"], p["kvs"], sel, p["B"], p["C"], p["scale"])
+        for (hi, g), r in rows.items():
+            assert np.all(o[r][:, hi * G:(hi + 1) * G] == 0.0)
+            assert np.all(np.isneginf(lse[r][:, hi * G:(hi + 1) * G]))
+        assert np.isfinite(o).all()
+    o, lse = O.forward_blocked(p["q"], p["k"], p["v"], p["cu"], p["kvs"], sel, p["B"], p["C"], p["scale"])
+    dq, dk, dv = O.backward_blocked(p["q"], p["k"], p["v"], o, p["do"], lse, p["cu"], p["kvs"], sel, p["B"],
+                                    p["C"], p["scale"])
+    do2 = p["do"].copy()
+    for (hi, g), r in rows.items():
+        assert np.all(dq[r][:, hi * G:(hi + 1) * G] == 0.0)
+        do2[np.ix_(r, np.arange(hi * G, (hi + 1) * G))] += 100.0
+    _, dk2, dv2 = O.backward_blocked(p["q"], p["k"], p["v"], o, do2, lse, p["cu"], p["kvs"], sel, p["B"],
+                                     p["C"], p["scale"])
+    assert np.array_equal(dk, dk2) and np.array_equal(dv, dv2)
