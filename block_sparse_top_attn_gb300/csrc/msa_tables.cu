@@ -5,6 +5,8 @@
 // Both builds are deterministic: counts are order-independent sums, and every
 // position-dependent write is ordered by a sequential walk over query chunks
 // within a scatter group plus exclusive prefix sums across groups.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -509,28 +511,67 @@ __global__ void __launch_bounds__(256) task_emit_kernel(TaskArgs a) {
 // Scratch of msa_build_k2q_noalloc, for callers that may not allocate device
 // memory.  Every device that loads the library holds one copy until exit.  In
 // host code the name is only a host-side stand-in for the symbol, so the
-// device address is looked up once per device and kept.
+// device address is looked up once per device and kept, together with the
+// unique ID of the CUDA context it was looked up in: after cudaDeviceReset a
+// new context (with the module loaded again, possibly elsewhere) gets a new
+// ID, and the address is looked up again.
 static __device__ __align__(256) uint8_t g_k2q_scratch[MSA_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-void* g_k2q_scratch_addr[kMaxDevices];
+struct ScratchAddr {
+  unsigned long long ctx_id = 0;
+  void* ptr = nullptr;
+};
+ScratchAddr g_k2q_scratch_addr[kMaxDevices];
 std::mutex g_k2q_scratch_mu;
 
-// Device address of g_k2q_scratch on the current device.
+// Unique ID of the calling thread's current CUDA context (driver entry points
+// looked up through the runtime, so the library needs no link to libcuda).
+int current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    cudaGetLastError();
+  });
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, id) != CUDA_SUCCESS)
+    return MSA_ERR_CUDA;
+  return MSA_OK;
+}
+
+// Device address of g_k2q_scratch in the current device's current context.
 int k2q_scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MSA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MSA_ERR_INVALID_ARGUMENT;
+  // No context may be current yet (the runtime binds the primary context on
+  // its first real call): then the lookup below binds it, and its ID is read
+  // after.
+  unsigned long long ctx_id = 0;
+  const bool have_ctx = current_context_id(&ctx_id) == MSA_OK;
   std::lock_guard<std::mutex> lk(g_k2q_scratch_mu);
-  if (!g_k2q_scratch_addr[dev]) {
+  ScratchAddr& e = g_k2q_scratch_addr[dev];
+  if (!have_ctx || !e.ptr || e.ctx_id != ctx_id) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_k2q_scratch) != cudaSuccess || !ptr) {
       cudaGetLastError();
       return MSA_ERR_CUDA;
     }
-    g_k2q_scratch_addr[dev] = ptr;
+    if (!have_ctx && current_context_id(&ctx_id) != MSA_OK) return MSA_ERR_CUDA;
+    e.ptr = ptr;
+    e.ctx_id = ctx_id;
   }
-  *out = g_k2q_scratch_addr[dev];
+  *out = e.ptr;
   return MSA_OK;
 }
 }  // namespace
@@ -643,8 +684,11 @@ int msa_build_k2q(const msa_problem* p, const int32_t* sel, int32_t* row_ptr, in
                                     blk_off, chunk_off, d_status);
   const size_t hist_bytes = sizeof(int) * NB;
   if (hist_bytes > 48 * 1024) {
-    cudaFuncSetAttribute(k2q_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes);
-    cudaFuncSetAttribute(k2q_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes);
+    if ((rc = cuda_status(cudaFuncSetAttribute(k2q_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)hist_bytes))) ||
+        (rc = cuda_status(cudaFuncSetAttribute(k2q_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)hist_bytes))))
+      return rc;
   }
   k2q_count_kernel<<<dim3((unsigned)nS, Hi), 256, hist_bytes, st>>>(a);
   const int64_t rows = (int64_t)Hi * NB;

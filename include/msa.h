@@ -150,7 +150,10 @@ int msa_build_k2q(const msa_problem* p, const int32_t* sel, int32_t* row_ptr, in
  *    131,072 tokens with 8 index heads needs about 8.5 MB.
  *  - The first call on a device looks up the array's device address (a
  *    runtime query made once per device, with that device current); make that
- *    first call before any stream capture begins.
+ *    first call before any stream capture begins.  The address is kept with
+ *    the ID of the CUDA context it belongs to: after cudaDeviceReset (a new
+ *    context, where the array may sit elsewhere) the next call looks it up
+ *    again, and that call too should come before any capture.
  *  - Every call uses the same array and it keeps what the last call left
  *    there; the build overwrites all of it before reading, so nothing in it
  *    needs to start at zero.  Calls whose kernels overlap on the GPU (other

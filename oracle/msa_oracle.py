@@ -97,7 +97,9 @@ def f64_to_bf16(x: np.ndarray) -> np.ndarray:
 
 
 def bf16_ulp(x: np.ndarray) -> np.ndarray:
-    """Spacing of bf16 numbers at |x| (8 significant bits), for normal |x|."""
+    """Spacing of bf16 numbers at |x| (8 significant bits): 2**(e - 7) for |x|
+    in [2**e, 2**(e+1)); below the smallest normal, the subnormal spacing
+    2**-133."""
     ax = np.maximum(np.abs(np.asarray(x, dtype=np.float64)), np.finfo(np.float32).tiny)
     return np.exp2(np.floor(np.log2(ax)) - 7.0)
 
@@ -364,11 +366,6 @@ def backward_blocked(q, k, v, o, do, lse, cu_seqlens, kv_doc_starts, sel, block,
                 dk[k0 + kp, hi] += dkc
                 dv[k0 + kp, hi] += dvc
     return dq, dk, dv
-
-
-def preprocess_delta(o, do) -> np.ndarray:
-    """D[t, h] = sum_d dO[t, h, d] * O[t, h, d] in float64."""
-    return np.sum(_heads(do) * _heads(o), axis=2)
 
 
 # ---------------------------------------------------------------------------

@@ -81,10 +81,15 @@ def test_tables_are_deterministic(B):
         bw = B.Backward(prob)
         bw.build_tables(t["sel"])
         torch.cuda.synchronize()
+        assert int(bw.status[0].item()) == 0
         n = bw.num_tasks()
-        outs.append((bw.q_indices.cpu().numpy().copy(), bw.task_meta[:n].cpu().numpy().copy()))
+        e = int(bw.row_ptr[:, -1].max().item())
+        outs.append((bw.row_ptr.cpu().numpy().copy(), bw.q_indices[:, :e].cpu().numpy().copy(),
+                     bw.task_meta[:n].cpu().numpy().copy(), bw.task_q_rows[:n].cpu().numpy().copy(),
+                     bw.task_q_pos[:n].cpu().numpy().copy(), bw.walk.cpu().numpy().copy()))
     for o in outs[1:]:
-        np.testing.assert_array_equal(o[1], outs[0][1])
+        for a, b in zip(o, outs[0]):
+            np.testing.assert_array_equal(a, b)
 
 
 @pytest.mark.parametrize("bad", ["range", "causal", "dup"])

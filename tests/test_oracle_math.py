@@ -142,12 +142,6 @@ def test_sparse_selection_matches_masked_sdpa(blocked):
     nc = [-(-int(n) // C) for n in np.diff(p["cu"])]
     goff = np.concatenate([[0], np.cumsum(nc)])
 
-    def mask_fn(d, n):
-        # key j visible to query i iff j <= i and block(j) is in the selection of chunk(i)
-        # (built by expanding a chunk x block membership table; head 0 and head 1 differ,
-        # so build per index head and let _torch_ref broadcast -- here Hi masks are stacked)
-        return None
-
     # torch reference per index head (masks differ per index head)
     T, Hq, D = p["q"].shape
     Hi = sel.shape[0]
@@ -263,6 +257,32 @@ def test_bf16_rounding_of_float64_between_neighbours():
     assert O.f64_to_bf16(np.array([mid - 2.0 ** -40]))[0] == 0x3F80
     assert O.f64_to_bf16(np.array([mid + 2.0 ** -40]))[0] == 0x3F81
     assert O.f64_to_bf16(np.array([mid]))[0] == 0x3F80          # tie -> even
+
+
+def _bf16_bits_to_f64_torch(bits):
+    """Decode bf16 bit patterns with torch (independent of the oracle's decoder)."""
+    return torch.from_numpy(np.asarray(bits, np.uint16).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def test_bf16_ulp_is_the_spacing_of_adjacent_bf16_values():
+    """bf16_ulp(x) must equal the gap between x and the next larger-magnitude
+    bf16 value, for every positive and negative exponent of the format,
+    including the subnormal range (spacing 2**-133) and zero."""
+    bits = np.arange(0, 0x7F7F, dtype=np.uint32)          # all finite non-negative bf16 but the largest
+    rng = np.random.default_rng(5)
+    pick = np.unique(np.concatenate([bits[::7], bits[:300], rng.choice(bits, 4000)])).astype(np.uint16)
+    x = _bf16_bits_to_f64_torch(pick)
+    nxt = _bf16_bits_to_f64_torch(pick + np.uint16(1))
+    spacing = nxt - x
+    np.testing.assert_array_equal(O.bf16_ulp(x), spacing)
+    np.testing.assert_array_equal(O.bf16_ulp(-x), spacing)
+    # values strictly inside a binade (not bf16 values themselves) have the binade's spacing
+    inner = x * (1.0 + rng.uniform(0, 2.0 ** -9, x.size))
+    normal = x >= 2.0 ** -126
+    np.testing.assert_array_equal(O.bf16_ulp(inner[normal]), spacing[normal])
+    # a few values written out: 1 -> 2**-7, 8 -> 2**-4 (so half an ulp is 0.03125 on [8, 16)), 0 -> 2**-133
+    np.testing.assert_array_equal(O.bf16_ulp(np.array([1.0, 1.5, 8.0, 15.9, 0.0])),
+                                  [2.0 ** -7, 2.0 ** -7, 2.0 ** -4, 2.0 ** -4, 2.0 ** -133])
 
 
 def test_empty_chunk_attends_nothing():
