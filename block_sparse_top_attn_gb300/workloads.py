@@ -243,6 +243,32 @@ def device_values(pb: Problem, device="cuda", seed: int = 0):
     return draw((T, Hq, D)), draw((W, Hkv, D)), draw((W, Hkv, D)), draw((T, Hq, D))
 
 
+INDEX_DIM = 128
+
+
+def index_values(pb: Problem, seed: int = 0, index_dim: int = INDEX_DIM):
+    """Index projections for the block scorer: per token and index head, an
+    index query and an index key, bf16 N(0, 1) as uint16 bit patterns of shape
+    [T, Hi, index_dim] each.  They come from their own generator
+    (``default_rng([seed, 1])``: index queries, then index keys), so drawing
+    them leaves every other input of the workload unchanged."""
+    rng = np.random.default_rng([seed, 1])
+    shape = (pb.total_tokens, pb.num_index_heads, index_dim)
+    return _normal_bf16(rng, shape), _normal_bf16(rng, shape)
+
+
+def device_index_values(pb: Problem, device="cuda", seed: int = 0, index_dim: int = INDEX_DIM):
+    """index_values drawn on the device with torch's seeded Philox generator
+    (same distribution; for workloads whose host draw is slow).  Returns torch
+    bf16 tensors (q_index, k_index)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed + 1_000_003)
+    shape = (pb.total_tokens, pb.num_index_heads, index_dim)
+    return tuple(torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+                 for _ in range(2))
+
+
 def effective_flops(pb: Problem) -> int:
     """Effective FLOP of the backward over full selected blocks: every
     (query, q-head, selected block) costs 5 GEMMs x 2 x block x head_dim."""

@@ -38,6 +38,10 @@ topology, the text of the problem statement states the math):
       dK_j = scale * sum_{i, h in group} dS_ij q_i,
       dV_j = sum_{i, h in group} P_ij dO_i.
 
+The block scorer that produces ``sel`` (``pool_index``, ``block_scores``,
+``select_topk``) follows a reading stated above its functions: the pages name
+the scorer and its index dimension but not the score.
+
 Readings where the pages are silent (each also listed in the design notes):
 block size B and chunk C are parameters (the configs use B = 64, C = 8);
 ``sel`` is int32 [Hi, NC, K] of document-local block ids with -1 for an empty
@@ -428,6 +432,82 @@ def sampled_key_grads(q, k, v, do, cu_seqlens, kv_doc_starts, sel, block, chunk,
 
 
 # ---------------------------------------------------------------------------
+# block scorer and top-k selection (produces sel)
+# ---------------------------------------------------------------------------
+#
+# The msa_bindings page names a scorer launcher (MSAKernels.fmha_sm100) among
+# the entry points and the msa_schedule page fixes INDEX_DIM = 128 per index
+# head, but neither says how a key block is scored.  The reading used here:
+#   * pooled index query of query chunk c:  the mean of the chunk's tokens'
+#     index queries; pooled index key of key block b: the mean of the block's
+#     tokens' index keys (both within the document; a partial last chunk or
+#     block averages the tokens it has);
+#   * each mean is an fp32 sum over the tokens in order, divided by the token
+#     count in fp32, and stored rounded to bf16, like every other tensor;
+#   * score(c, b) = the fp32 dot product of the two pooled bf16 vectors,
+#     accumulated over the index dims in ascending order (every product of two
+#     bf16 values is exact in fp32, so this is a fixed sequence of rounded
+#     fp32 additions);
+#   * the diagonal block b = (first position of c) // B is always selected
+#     first; the other K - 1 slots take the causal blocks b < diagonal with the
+#     highest scores, a tie going to the lower block; the row of sel lists the
+#     diagonal, then those blocks by descending score, then -1 pads.
+
+def pool_index(x_bits, cu_seqlens, size: int) -> np.ndarray:
+    """Mean over consecutive groups of ``size`` tokens of each document.
+
+    x_bits: bf16 bits [T, Hi, D].  Returns bf16 bits [Hi, n_groups, D], groups
+    numbered document by document (so chunks for size = C, blocks for size = B).
+    """
+    x = bf16_to_f64(np.asarray(x_bits)).astype(np.float32)        # exact
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    T, Hi, D = x.shape
+    out = []
+    for d in range(len(cu) - 1):
+        t0, n = int(cu[d]), int(cu[d + 1] - cu[d])
+        for g0 in range(0, n, size):
+            rows = range(t0 + g0, t0 + min(g0 + size, n))
+            acc = np.zeros((Hi, D), dtype=np.float32)
+            for t in rows:                                        # fp32 adds in token order
+                acc = acc + x[t]
+            mean = acc / np.float32(len(rows))                    # fp32 division, correctly rounded
+            out.append(f64_to_bf16(mean.astype(np.float64)))
+    return np.stack(out, axis=1)
+
+
+def block_scores(qpool_bits, kpool_bits) -> np.ndarray:
+    """fp32 scores [..., nq, nk] of pooled queries [..., nq, D] against pooled
+    keys [..., nk, D] (bf16 bits), accumulated over D in ascending order."""
+    qp = bf16_to_f64(np.asarray(qpool_bits)).astype(np.float32)
+    kp = bf16_to_f64(np.asarray(kpool_bits)).astype(np.float32)
+    acc = np.zeros(qp.shape[:-1] + (kp.shape[-2],), dtype=np.float32)
+    for i in range(qp.shape[-1]):
+        acc = acc + qp[..., :, None, i] * kp[..., None, :, i]     # exact products, rounded sums
+    return acc
+
+
+def select_topk(q_index, k_index, cu_seqlens, block: int, chunk: int, topk: int) -> np.ndarray:
+    """sel int32 [Hi, NC, K] from index projections q_index, k_index (bf16 bits
+    [T, Hi, D]) by the scorer reading above."""
+    lay = DocLayout(cu_seqlens, block, chunk)
+    qpool = pool_index(q_index, cu_seqlens, chunk)                 # [Hi, NC, D]
+    kpool = pool_index(k_index, cu_seqlens, block)                 # [Hi, NB, D]
+    Hi = qpool.shape[0]
+    sel = np.full((Hi, lay.NC, topk), -1, dtype=np.int32)
+    for d in range(lay.num_docs):
+        g0, r0 = int(lay.chunk_off[d]), int(lay.blk_off[d])
+        nc, nb = int(lay.nc[d]), int(lay.nb[d])
+        for hi in range(Hi):
+            sc = block_scores(qpool[hi, g0:g0 + nc], kpool[hi, r0:r0 + nb])   # [nc, nb]
+            for c in range(nc):
+                diag = (c * chunk) // block
+                ranked = sorted(range(diag), key=lambda b: (-float(sc[c, b]), b))[:topk - 1]
+                row = [diag] + ranked
+                sel[hi, g0 + c, :len(row)] = row
+    return sel
+
+
+# ---------------------------------------------------------------------------
 # index tables: key-block -> query CSR, task rows, CTA walk
 # ---------------------------------------------------------------------------
 
@@ -523,6 +603,40 @@ def build_tasks(row_ptr, q_indices, cu_seqlens, block, chunk, tile_chunks=0):
     q_pos = np.where(valid, pos, -1).astype(np.int32)
     q_rows = np.where(valid, lay.cu[d][:, None] + pos, -1).astype(np.int32)
     return meta.reshape(n, 6), q_rows.reshape(n, chunk), q_pos.reshape(n, chunk)
+
+
+def plan_forward(sel, cu_seqlens, block: int, chunk: int):
+    """Forward work plan (the planner launcher of the msa_bindings page,
+    MSAKernels.fmha_sm100_plan; scheduler_metadata and work_count of the
+    msa_schedule page).
+
+    One work item per (index head, query chunk), in the scheduler_metadata
+    column order (index_head, row_linear, q_begin, q_count, document_ordinal,
+    document_local_kblock) read for query-chunk items: row_linear is the global
+    chunk, q_begin its first token row, q_count its token count, and
+    document_local_kblock the document-local key block holding its first query
+    (its diagonal block).  Items are ordered longest first: descending number
+    of selected blocks, ties in (index head, chunk) order; items that select no
+    block come last.  Returns (meta int32 [Hi * NC, 6], work_count = number of
+    items that select at least one block).
+    """
+    sel = np.asarray(sel)
+    lay = DocLayout(cu_seqlens, block, chunk)
+    Hi = sel.shape[0]
+    items = []
+    for hi in range(Hi):
+        for d in range(lay.num_docs):
+            for c in range(int(lay.nc[d])):
+                g = int(lay.chunk_off[d]) + c
+                nsel = int((sel[hi, g] >= 0).sum())
+                q0 = c * chunk
+                row = (hi, g, int(lay.cu[d]) + q0, min(chunk, int(lay.lengths[d]) - q0), d, q0 // block)
+                items.append((nsel, row))
+    # stable: sorted() keeps the (index head, chunk) order among equal counts
+    items = sorted(items, key=lambda it: -it[0])
+    meta = np.array([row for _, row in items], dtype=np.int32).reshape(-1, 6)
+    work = sum(1 for n, _ in items if n > 0)
+    return meta, work
 
 
 def rows_per_cta(num_rows: int) -> int:

@@ -145,3 +145,31 @@ def test_named_workload_task_counts(name, tasks):
     pb = W.make_problem(name, values=False)
     # one task per valid (index head, chunk, block) selection entry
     assert int((pb.sel >= 0).sum()) == tasks
+
+
+def test_forward_plan_orders_longest_first_and_counts_nonempty_items():
+    """The forward plan is a permutation of every (index head, chunk) item,
+    ordered by descending selected-block count with ties in (head, chunk)
+    order (checked against numpy's lexsort), empty items last, and work_count
+    counts the non-empty ones; each row's columns follow from the layout."""
+    from block_sparse_top_attn_gb300 import workloads as W
+    pb = W.make_problem(lengths=[200, 77, 130, 1, 9, 513], num_index_heads=2, topk=5, policy="diag_uniform",
+                        seed=3, values=False)
+    sel = pb.sel.copy()
+    sel[1, 10:14] = -1                                  # a few chunks that select nothing
+    meta, work = O.plan_forward(sel, pb.cu_seqlens, pb.block, pb.chunk)
+    lay = O.DocLayout(pb.cu_seqlens, pb.block, pb.chunk)
+    Hi, NC = sel.shape[:2]
+    nsel = (sel >= 0).sum(axis=2)                       # [Hi, NC]
+    hh, gg = np.meshgrid(np.arange(Hi), np.arange(NC), indexing="ij")
+    order = np.lexsort((gg.ravel(), hh.ravel(), -nsel.ravel()))
+    np.testing.assert_array_equal(meta[:, 0], hh.ravel()[order])
+    np.testing.assert_array_equal(meta[:, 1], gg.ravel()[order])
+    assert work == int((nsel > 0).sum()) == Hi * NC - 4
+    assert (nsel[meta[work:, 0], meta[work:, 1]] == 0).all()
+    for hi, g, q_begin, q_count, d, kb in meta:
+        c = g - lay.chunk_off[d]
+        assert lay.chunk_off[d] <= g < lay.chunk_off[d] + lay.nc[d]
+        assert q_begin == lay.cu[d] + c * pb.chunk
+        assert q_count == min(pb.chunk, lay.lengths[d] - c * pb.chunk)
+        assert kb == c * pb.chunk // pb.block
