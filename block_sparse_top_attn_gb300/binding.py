@@ -83,6 +83,9 @@ def _load():
         "msa_device_sm_count": (ctypes.c_int, [i32, ctypes.POINTER(i32)]),
         "msa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "msa_selftest_wait_timeout": (ctypes.c_int, [vp, vp]),
+        "msa_select_topk": (ctypes.c_int, [P, vp, vp, vp, vp, vp, sz, vp]),
+        "msa_plan_forward": (ctypes.c_int, [P, vp, vp, vp, vp, vp, sz, vp]),
+        "msa_fwd_planned": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -291,6 +294,52 @@ def msa_fwd(p: Problem, q, k, v, sel, o, lse, d_status, ws, stream=None):
            "msa_fwd")
 
 
+def msa_select_topk(p: Problem, q_index, k_index, sel, d_status, ws, stream=None):
+    s = p.c_struct()
+    _check(lib.msa_select_topk(ctypes.byref(s), _ptr(q_index), _ptr(k_index), _ptr(sel), _ptr(d_status), _ptr(ws),
+                               ws.numel() * ws.element_size(), _stream(stream)),
+           "msa_select_topk")
+
+
+def msa_plan_forward(p: Problem, sel, scheduler_metadata, work_count, d_status, ws, stream=None):
+    s = p.c_struct()
+    _check(lib.msa_plan_forward(ctypes.byref(s), _ptr(sel), _ptr(scheduler_metadata), _ptr(work_count),
+                                _ptr(d_status), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "msa_plan_forward")
+
+
+def msa_fwd_planned(p: Problem, q, k, v, sel, scheduler_metadata, o, lse, d_status, ws, stream=None):
+    s = p.c_struct()
+    _check(lib.msa_fwd_planned(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(sel), _ptr(scheduler_metadata),
+                               _ptr(o), _ptr(lse), _ptr(d_status), _ptr(ws), ws.numel() * ws.element_size(),
+                               _stream(stream)),
+           "msa_fwd_planned")
+
+
+def plan_forward(p: Problem, sel, stream=None):
+    """msa_plan_forward convenience: returns (scheduler_metadata [Hi*NC, 6],
+    work_count [1], status tensor)."""
+    import torch
+    dev = p.d_cu.device
+    meta = torch.empty((p.num_index_heads * p.num_chunks, MSA_TASK_META_COLS), dtype=torch.int32, device=dev)
+    wc = torch.zeros(4, dtype=torch.int32, device=dev)
+    st = torch.zeros(4, dtype=torch.int32, device=dev)
+    ws = torch.empty(msa_workspace_bytes(p, 1, 1, 0), dtype=torch.uint8, device=dev)
+    msa_plan_forward(p, sel, meta, wc, st, ws, stream)
+    return meta, wc, st
+
+
+def select_topk(p: Problem, q_index, k_index, stream=None):
+    """msa_select_topk convenience: returns (sel int32 [Hi, NC, topk], status tensor)."""
+    import torch
+    dev = p.d_cu.device
+    sel = torch.empty((p.num_index_heads, p.num_chunks, p.topk), dtype=torch.int32, device=dev)
+    st = torch.zeros(4, dtype=torch.int32, device=dev)
+    ws = torch.empty(msa_workspace_bytes(p, 1, 1, 0), dtype=torch.uint8, device=dev)
+    msa_select_topk(p, q_index, k_index, sel, st, ws, stream)
+    return sel, st
+
+
 # ---------------------------------------------------------------------------
 # convenience: one problem's buffers and the whole backward sequence
 # ---------------------------------------------------------------------------
@@ -357,13 +406,18 @@ class Backward:
         return int(self.walk[0].item())
 
 
-def forward(p: Problem, sel, q, k, v, stream=None):
-    """msa_fwd convenience: returns (o bf16 [T, Hq, 128], lse fp32 [T, Hq], status tensor)."""
+def forward(p: Problem, sel, q, k, v, stream=None, plan=None):
+    """msa_fwd convenience (msa_fwd_planned when plan, a scheduler_metadata
+    tensor from plan_forward, is given): returns (o bf16 [T, Hq, 128], lse fp32
+    [T, Hq], status tensor)."""
     import torch
     dev = p.d_cu.device
     o = torch.empty((p.total_tokens, p.num_q_heads, HEAD_DIM), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((p.total_tokens, p.num_q_heads), dtype=torch.float32, device=dev)
     st = torch.zeros(4, dtype=torch.int32, device=dev)
     ws = torch.empty(max(256, 8 * (p.num_docs + 1) + 256), dtype=torch.uint8, device=dev)
-    msa_fwd(p, q, k, v, sel, o, lse, st, ws, stream)
+    if plan is None:
+        msa_fwd(p, q, k, v, sel, o, lse, st, ws, stream)
+    else:
+        msa_fwd_planned(p, q, k, v, sel, plan, o, lse, st, ws, stream)
     return o, lse, st

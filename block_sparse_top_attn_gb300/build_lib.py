@@ -14,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmsa.so")
-SOURCES = ["msa_tables.cu", "msa_bwd.cu", "msa_fwd.cu"]
+SOURCES = ["msa_tables.cu", "msa_bwd.cu", "msa_fwd.cu", "msa_score.cu"]
 HEADERS = ["msa_common.cuh", "msa_host.cuh", "msa_tmap.cuh", "msa_bwd_ws.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -86,6 +86,7 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
 
 struct FwdArgs {
   const int32_t* sel;
+  const int32_t* plan;  // scheduler_metadata rows of a forward plan, or null: items in index order
   const int32_t* cu;
   const int32_t* chunk_off;
   uint16_t* o;
@@ -168,7 +169,10 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
   bool aborted = status_bad(a.status);
   const int64_t items = (int64_t)a.Hi * a.NC;
   for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
-    const int hi = (int)(w / a.NC), g = (int)(w % a.NC);
+    // the walk's w-th item: the plan's row w (a permutation of the items,
+    // longest first), or item w itself
+    const int hi = a.plan ? a.plan[w * MSA_TASK_META_COLS] : (int)(w / a.NC);
+    const int g = a.plan ? a.plan[w * MSA_TASK_META_COLS + 1] : (int)(w % a.NC);
     const int d = doc_of_chunk(a.chunk_off, a.N + 1, g);
     if (warp == kIssueWarp) {  // compact the item's selection, order kept
       const int b = lane < a.K ? a.sel[((int64_t)hi * a.NC + g) * a.K + lane] : -1;
@@ -422,11 +426,12 @@ __global__ void layout_kernel(const int32_t* cu, const int32_t* kvs, int N, int 
 
 using namespace msa;
 
-extern "C" int msa_fwd(const msa_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                       const int32_t* sel, uint16_t* o, float* lse, int32_t* d_status, void* ws, size_t ws_bytes,
-                       void* stream) {
+static int launch_fwd(const msa_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                      const int32_t* sel, const int32_t* plan, uint16_t* o, float* lse, int32_t* d_status, void* ws,
+                      size_t ws_bytes, void* stream) {
   int rc = check_problem(p);
   if (rc) return rc;
+  if (plan && !aligned16(plan)) return MSA_ERR_INVALID_ARGUMENT;
   const void* ptrs[] = {q, k, v, sel, o, lse, d_status, ws};
   for (const void* x : ptrs)
     if (!x || !aligned16(x)) return MSA_ERR_INVALID_ARGUMENT;
@@ -451,7 +456,7 @@ extern "C" int msa_fwd(const msa_problem* p, const uint16_t* q, const uint16_t* 
                            (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     return MSA_ERR_CUDA;
   FwdArgs a;
-  a.sel = sel; a.cu = p->cu_seqlens; a.chunk_off = chunk_off; a.o = o; a.lse = lse; a.N = N;
+  a.sel = sel; a.plan = plan; a.cu = p->cu_seqlens; a.chunk_off = chunk_off; a.o = o; a.lse = lse; a.N = N;
   a.NC = p->num_chunks; a.K = p->topk; a.Hi = p->num_index_heads; a.Hq = (int)Hq;
   a.scale_log2 = p->softmax_scale * fwd::kLog2e; a.status = d_status;
   const int64_t items = (int64_t)p->num_index_heads * p->num_chunks;
@@ -469,4 +474,17 @@ extern "C" int msa_fwd(const msa_problem* p, const uint16_t* q, const uint16_t* 
   const int grid = (int)(items < slots ? items : slots);
   fwd_kernel<<<grid, fwd::kThreads, fwd::SMEM, st>>>(tmQ, tmK, tmV, p->kv_doc_starts, a);
   return cuda_status(cudaGetLastError());
+}
+
+extern "C" int msa_fwd(const msa_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       const int32_t* sel, uint16_t* o, float* lse, int32_t* d_status, void* ws, size_t ws_bytes,
+                       void* stream) {
+  return launch_fwd(p, q, k, v, sel, nullptr, o, lse, d_status, ws, ws_bytes, stream);
+}
+
+extern "C" int msa_fwd_planned(const msa_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               const int32_t* sel, const int32_t* scheduler_metadata, uint16_t* o, float* lse,
+                               int32_t* d_status, void* ws, size_t ws_bytes, void* stream) {
+  if (!scheduler_metadata) return MSA_ERR_INVALID_ARGUMENT;
+  return launch_fwd(p, q, k, v, sel, scheduler_metadata, o, lse, d_status, ws, ws_bytes, stream);
 }

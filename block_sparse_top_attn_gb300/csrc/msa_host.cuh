@@ -34,6 +34,11 @@ inline int64_t num_tiles(int64_t nc, int32_t tile_chunks) {
 }
 
 size_t k2q_ws_bytes(const msa_problem* p);
+size_t select_ws_bytes(const msa_problem* p);
+// Launches the document-layout kernel: blk_off[d], chunk_off[d] for d in
+// [0, N] (device int32 [N+1] each) and the consistency checks of cu_seqlens
+// and kv_doc_starts (MSA_ERR_INVALID_DOCUMENTS in *status).
+int launch_layout(const msa_problem* p, int32_t* blk_off, int32_t* chunk_off, int32_t* status, cudaStream_t st);
 size_t tasks_ws_bytes(const msa_problem* p, int32_t tile_chunks);
 size_t bwd_ws_bytes(const msa_problem* p);
 

@@ -49,6 +49,14 @@ size_t k2q_ws_bytes(const msa_problem* p) {
   return b;
 }
 
+size_t select_ws_bytes(const msa_problem* p) {
+  const int64_t Hi = p->num_index_heads, NB = p->num_blocks, NC = p->num_chunks, N = p->num_docs;
+  size_t b = round_up(sizeof(int32_t) * 2 * (N + 1), 256);
+  b += round_up(sizeof(uint16_t) * Hi * NC * kHeadDim, 256);   // pooled index queries
+  b += round_up(sizeof(uint16_t) * Hi * NB * kHeadDim, 256);   // pooled index keys
+  return b;
+}
+
 static constexpr int kScanSeg = 2048;  // elements per block of the multi-block scan
 
 size_t tasks_ws_bytes(const msa_problem* p, int32_t tile_chunks) {
@@ -329,7 +337,15 @@ __global__ void __launch_bounds__(32) k2q_scatter_kernel(K2QArgs a) {
     }
     __syncwarp();
     if (p >= 0 && (int64_t)p + len <= a.edge_cap) {
-      for (int i = 0; i < len; ++i) qi[p + i] = c * kChunk + i;
+      int32_t* dst = qi + p;
+      const int v0 = c * kChunk;
+      if (len == kChunk && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+        // a full chunk at a 16-byte boundary: two vector stores
+        reinterpret_cast<int4*>(dst)[0] = make_int4(v0, v0 + 1, v0 + 2, v0 + 3);
+        reinterpret_cast<int4*>(dst)[1] = make_int4(v0 + 4, v0 + 5, v0 + 6, v0 + 7);
+      } else {
+        for (int i = 0; i < len; ++i) dst[i] = v0 + i;
+      }
     }
   }
 }
@@ -485,15 +501,23 @@ __global__ void __launch_bounds__(256) task_emit_kernel(TaskArgs a) {
     if (act) {
       const int64_t t = (int64_t)a.toff[((int64_t)hi * a.ntiles + tile) * a.NB + r] + (k - start_k);
       if (t < a.task_cap) {
-        int32_t* mt = a.meta + t * MSA_TASK_META_COLS;
-        mt[0] = hi; mt[1] = r; mt[2] = s; mt[3] = cnt; mt[4] = d; mt[5] = b;
+        // a meta row is 24 bytes: three 8-byte stores (t * 24 is a multiple of 8)
+        int2* mt = reinterpret_cast<int2*>(a.meta + t * MSA_TASK_META_COLS);
+        mt[0] = make_int2(hi, r);
+        mt[1] = make_int2(s, cnt);
+        mt[2] = make_int2(d, b);
         int rows[kChunk], pos[kChunk];
+        const int32_t* src = qi + s;
+        if (cnt == kChunk && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+          const int4 x0 = reinterpret_cast<const int4*>(src)[0], x1 = reinterpret_cast<const int4*>(src)[1];
+          pos[0] = x0.x; pos[1] = x0.y; pos[2] = x0.z; pos[3] = x0.w;
+          pos[4] = x1.x; pos[5] = x1.y; pos[6] = x1.z; pos[7] = x1.w;
+        } else {
 #pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-          const int pi = i < cnt ? qi[s + i] : -1;
-          pos[i] = pi;
-          rows[i] = i < cnt ? tok0 + pi : -1;
+          for (int i = 0; i < kChunk; ++i) pos[i] = i < cnt ? src[i] : -1;
         }
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) rows[i] = i < cnt ? tok0 + pos[i] : -1;
         int4* qr = reinterpret_cast<int4*>(a.q_rows + t * kChunk);
         int4* qp = reinterpret_cast<int4*>(a.q_pos + t * kChunk);
         qr[0] = make_int4(rows[0], rows[1], rows[2], rows[3]);
@@ -506,6 +530,101 @@ __global__ void __launch_bounds__(256) task_emit_kernel(TaskArgs a) {
     prev_tile = __shfl_sync(0xffffffffu, tile, last);
     prev_start = __shfl_sync(0xffffffffu, start_k, last);
   }
+}
+
+// ---------------------------------------------------------------------------
+// forward work plan: a stable counting sort of the (index head, chunk) items by
+// selected-block count, longest first, items selecting nothing last
+// ---------------------------------------------------------------------------
+constexpr int kPlanBlock = 1024;         // items per block of the plan kernels
+constexpr int kPlanBins = kMaxTopk + 1;  // selected-block counts 0 .. 32
+
+struct PlanArgs {
+  const int32_t* sel;
+  const int32_t* cu;
+  const int32_t* chunk_off;
+  int32_t* hist;       // [nblk][kPlanBins]: counts, then exclusive output offsets
+  int32_t* meta;       // [Hi * NC, 6]
+  int32_t* work_count;
+  int N, NC, K, Hi, nblk;
+  int32_t* status;
+};
+
+// Bin of an item in output order: count K first, ..., count 1, then count 0.
+__device__ __forceinline__ int plan_bin(int nsel, int K) { return nsel > 0 ? K - nsel : K; }
+
+__device__ __forceinline__ int plan_nsel(const PlanArgs& a, int64_t item) {
+  const int hi = (int)(item / a.NC), g = (int)(item % a.NC);
+  int n = 0;
+  const int32_t* row = a.sel + ((int64_t)hi * a.NC + g) * a.K;
+  for (int k = 0; k < a.K; ++k) n += row[k] >= 0;
+  return n;
+}
+
+__global__ void __launch_bounds__(kPlanBlock) plan_hist_kernel(PlanArgs a) {
+  __shared__ int h[kPlanBins];
+  if (status_bad(a.status)) return;
+  if (threadIdx.x < kPlanBins) h[threadIdx.x] = 0;
+  __syncthreads();
+  const int64_t item = (int64_t)blockIdx.x * kPlanBlock + threadIdx.x;
+  if (item < (int64_t)a.Hi * a.NC) atomicAdd(&h[plan_bin(plan_nsel(a, item), a.K)], 1);
+  __syncthreads();
+  if (threadIdx.x < kPlanBins) a.hist[(int64_t)blockIdx.x * kPlanBins + threadIdx.x] = h[threadIdx.x];
+}
+
+// One block: output offset of every (block, bin) = items of earlier bins plus
+// items of the same bin in earlier blocks; work_count = items of bins with a
+// selected block.
+__global__ void __launch_bounds__(1024) plan_scan_kernel(PlanArgs a) {
+  __shared__ int ws[32];
+  __shared__ int tot;
+  if (status_bad(a.status)) return;
+  int64_t carry = 0;
+  for (int bin = 0; bin <= a.K; ++bin) {
+    if (bin == a.K && threadIdx.x == 0) *a.work_count = (int32_t)carry;
+    for (int base = 0; base < a.nblk; base += 1024) {
+      const int b = base + threadIdx.x;
+      const int v = b < a.nblk ? a.hist[(int64_t)b * kPlanBins + bin] : 0;
+      const int e = block_excl_scan(v, ws, &tot);
+      if (b < a.nblk) a.hist[(int64_t)b * kPlanBins + bin] = (int32_t)(carry + e);
+      carry += tot;
+    }
+  }
+}
+
+// Each item's position: its block's offset for its bin plus its rank among the
+// block's earlier items of the same bin (stable).
+__global__ void __launch_bounds__(kPlanBlock) plan_scatter_kernel(PlanArgs a) {
+  __shared__ int wcount[kPlanBlock / 32][kPlanBins];
+  if (status_bad(a.status)) return;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < (kPlanBlock / 32) * kPlanBins; i += kPlanBlock) (&wcount[0][0])[i] = 0;
+  __syncthreads();
+  const int64_t item = (int64_t)blockIdx.x * kPlanBlock + threadIdx.x;
+  const bool valid = item < (int64_t)a.Hi * a.NC;
+  const int bin = valid ? plan_bin(plan_nsel(a, item), a.K) : kPlanBins;  // kPlanBins: no bin
+  const unsigned same = __match_any_sync(0xffffffffu, bin);
+  const int rank_in_warp = __popc(same & ((1u << lane) - 1u));
+  if (valid && rank_in_warp == 0) wcount[w][bin] = __popc(same);
+  __syncthreads();
+  if (!valid) return;
+  int before = 0;
+  for (int v = 0; v < w; ++v) before += wcount[v][bin];
+  const int64_t pos = a.hist[(int64_t)blockIdx.x * kPlanBins + bin] + before + rank_in_warp;
+  const int hi = (int)(item / a.NC), g = (int)(item % a.NC);
+  const int d = upper_index(a.chunk_off, a.N + 1, g);
+  const int c = g - a.chunk_off[d];
+  const int len = a.cu[d + 1] - a.cu[d];
+  int2* mt = reinterpret_cast<int2*>(a.meta + pos * MSA_TASK_META_COLS);
+  mt[0] = make_int2(hi, g);
+  mt[1] = make_int2(a.cu[d] + c * kChunk, min(kChunk, len - c * kChunk));
+  mt[2] = make_int2(d, c * kChunk / kBlock);
+}
+
+size_t plan_ws_bytes(const msa_problem* p) {
+  const int64_t items = (int64_t)p->num_index_heads * p->num_chunks, N = p->num_docs;
+  const int64_t nblk = (items + kPlanBlock - 1) / kPlanBlock;
+  return round_up(sizeof(int32_t) * 2 * (N + 1), 256) + round_up(sizeof(int32_t) * nblk * kPlanBins, 256);
 }
 
 // Scratch of msa_build_k2q_noalloc, for callers that may not allocate device
@@ -576,6 +695,14 @@ int k2q_scratch_address(void** out) {
 }
 }  // namespace
 
+}  // namespace msa
+
+namespace msa {
+int launch_layout(const msa_problem* p, int32_t* blk_off, int32_t* chunk_off, int32_t* status, cudaStream_t st) {
+  layout_kernel<<<1, 1024, 0, st>>>(p->cu_seqlens, p->kv_doc_starts, p->num_docs, p->total_tokens, p->kv_rows,
+                                    p->num_blocks, p->num_chunks, blk_off, chunk_off, status);
+  return cuda_status(cudaGetLastError());
+}
 }  // namespace msa
 
 using namespace msa;
@@ -650,9 +777,11 @@ int msa_device_sm_count(int32_t device, int32_t* sms) {
 
 size_t msa_workspace_bytes(const msa_problem* p, int64_t edge_cap, int64_t task_cap, int32_t tile_chunks) {
   if (check_problem(p) != MSA_OK || edge_cap < 0 || task_cap < 0 || tile_chunks < 0) return 0;
-  size_t a = k2q_ws_bytes(p), b = tasks_ws_bytes(p, tile_chunks), c = bwd_ws_bytes(p);
-  size_t m = a > b ? a : b;
-  return m > c ? m : c;
+  const size_t sizes[] = {k2q_ws_bytes(p), tasks_ws_bytes(p, tile_chunks), bwd_ws_bytes(p), select_ws_bytes(p),
+                          plan_ws_bytes(p)};
+  size_t m = 0;
+  for (size_t x : sizes) m = x > m ? x : m;
+  return m;
 }
 
 int msa_build_k2q(const msa_problem* p, const int32_t* sel, int32_t* row_ptr, int32_t* q_indices,
@@ -758,6 +887,35 @@ int msa_build_tasks(const msa_problem* p, const int32_t* row_ptr, const int32_t*
   scan_bsums_walk_kernel<<<1, 1024, 0, st>>>(a.bsum, nblk, a);
   scan_apply_kernel<<<nblk, 1024, 0, st>>>(a.tcnt, n, a.bsum, a.toff, d_status);
   task_emit_kernel<<<blocks, 256, 0, st>>>(a);
+  return cuda_status(cudaGetLastError());
+}
+
+int msa_plan_forward(const msa_problem* p, const int32_t* sel, int32_t* scheduler_metadata, int32_t* work_count,
+                     int32_t* d_status, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_problem(p);
+  if (rc) return rc;
+  if (!sel || !scheduler_metadata || !work_count || !d_status || !ws) return MSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(sel) || !aligned16(scheduler_metadata) || !aligned16(work_count) || !aligned16(d_status) ||
+      !aligned16(ws))
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (ws_bytes < plan_ws_bytes(p)) return MSA_ERR_INVALID_ARGUMENT;
+  if ((rc = check_device_current())) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int N = p->num_docs;
+  const int64_t items = (int64_t)p->num_index_heads * p->num_chunks;
+  if (items > INT32_MAX / 2) return MSA_ERR_UNSUPPORTED_SHAPE;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* blk_off = reinterpret_cast<int32_t*>(w);
+  int32_t* chunk_off = blk_off + (N + 1);
+  w += round_up(sizeof(int32_t) * 2 * (N + 1), 256);
+  PlanArgs a;
+  a.sel = sel; a.cu = p->cu_seqlens; a.chunk_off = chunk_off; a.hist = reinterpret_cast<int32_t*>(w);
+  a.meta = scheduler_metadata; a.work_count = work_count; a.N = N; a.NC = p->num_chunks; a.K = p->topk;
+  a.Hi = p->num_index_heads; a.nblk = (int)((items + kPlanBlock - 1) / kPlanBlock); a.status = d_status;
+  if ((rc = launch_layout(p, blk_off, chunk_off, d_status, st))) return rc;
+  plan_hist_kernel<<<a.nblk, kPlanBlock, 0, st>>>(a);
+  plan_scan_kernel<<<1, 1024, 0, st>>>(a);
+  plan_scatter_kernel<<<a.nblk, kPlanBlock, 0, st>>>(a);
   return cuda_status(cudaGetLastError());
 }
 

@@ -238,6 +238,61 @@ int msa_fwd(const msa_problem* p, const uint16_t* q, const uint16_t* k, const ui
             const int32_t* sel, uint16_t* o, float* lse, int32_t* d_status, void* ws,
             size_t ws_bytes, void* stream);
 
+/* Block scorer and top-k selection: writes the sel array that msa_build_k2q
+ * and msa_fwd consume ("msa_bindings" page, MSAKernels.fmha_sm100, the scorer
+ * launcher; "msa_schedule" page, INDEX_DIM = 128 index dims per index head).
+ * The pages name the scorer but not its score; this call computes:
+ *  - per index head, the pooled index query of every query chunk and the
+ *    pooled index key of every key block: the mean of the tokens' index
+ *    vectors inside the document (fp32 sum in token order, divided by the
+ *    token count, rounded to bf16);
+ *  - score(chunk, block) = the fp32 dot product of the two pooled vectors,
+ *    summed in ascending index-dim order;
+ *  - sel[hi][g] = the chunk's diagonal block (the one holding its first
+ *    query), then the topk - 1 blocks before it with the highest scores (a tie
+ *    goes to the lower block) by descending score, then -1; every entry is a
+ *    document-local block id and causal, so the result is a valid selection.
+ * q_index, k_index  device bf16 [T, Hi, 128]: index query / key of each token
+ *                   (compact token rows, the cu_seqlens order).
+ * sel               device int32 [Hi, NC, topk] out.
+ * ws                device workspace of at least msa_workspace_bytes() bytes
+ *                   (it holds the pooled vectors).
+ * Deterministic: the same inputs give the same sel on every run.  Returns
+ * MSA_ERR_INVALID_ARGUMENT for a null or misaligned pointer or a short ws;
+ * device-detected document errors go to *d_status.  Asynchronous on stream. */
+int msa_select_topk(const msa_problem* p, const uint16_t* q_index, const uint16_t* k_index, int32_t* sel,
+                    int32_t* d_status, void* ws, size_t ws_bytes, void* stream);
+
+/* Forward work plan ("msa_bindings" page, MSAKernels.fmha_sm100_plan, the
+ * planner launcher; "msa_schedule" page, MSABackwardSchedule's
+ * scheduler_metadata and work_count): the forward's work items, built on the
+ * device with no host synchronisation.
+ * One item per (index head, query chunk), written as a scheduler_metadata row
+ * in the pages' column order (MSA_TASK_META_COLS): index_head, row_linear =
+ * the global query chunk, q_begin = its first token row, q_count = its token
+ * count, document_ordinal, document_local_kblock = the key block holding its
+ * first query.  Rows are ordered longest first: descending number of selected
+ * blocks, ties in (index head, chunk) order, items selecting no block last, so
+ * a persistent walk over them meets the long items first.
+ * sel                 device int32 [Hi, NC, K], as for msa_fwd.
+ * scheduler_metadata  device int32 [Hi * NC, 6] out: every item, once.
+ * work_count          device int32 [1] out: items that select at least one
+ *                     block (the rows before the empty ones).
+ * ws                  workspace of at least msa_workspace_bytes() bytes.
+ * Deterministic.  Asynchronous on stream; argument errors are return codes,
+ * document errors go to *d_status. */
+int msa_plan_forward(const msa_problem* p, const int32_t* sel, int32_t* scheduler_metadata,
+                     int32_t* work_count, int32_t* d_status, void* ws, size_t ws_bytes, void* stream);
+
+/* msa_fwd walking the items in the order of a plan written by
+ * msa_plan_forward for the same problem and selection (the w-th item the
+ * persistent CTAs take is row w of scheduler_metadata).  O and LSE are the
+ * same, bit for bit, as msa_fwd's: every item is computed the same way
+ * whichever CTA takes it. */
+int msa_fwd_planned(const msa_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                    const int32_t* sel, const int32_t* scheduler_metadata, uint16_t* o, float* lse,
+                    int32_t* d_status, void* ws, size_t ws_bytes, void* stream);
+
 /* Self-test of the bounded device waits (no counterpart in the pages).
  * Launches one small kernel that waits, with the same bounded mbarrier wait
  * every kernel of this library uses, for an mbarrier phase that nothing
