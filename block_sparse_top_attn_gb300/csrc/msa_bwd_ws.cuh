@@ -37,6 +37,9 @@
 //
 // Every mbarrier wait is bounded (kWaitLimitNs) and also gives up when any
 // role has raised the shared abort flag; the status word records the timeout.
+// On the way out the TMA producer waits (bounded, ignoring the abort flag) for
+// every load it issued, so no copy still writes shared memory when the CTA
+// exits; the issuers wait for their last MMAs before TMEM is freed.
 #pragma once
 
 namespace msa {
@@ -281,6 +284,9 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         // query tile (they stay in L2 while the CTAs walk the tile together);
         // a K/V tile only within its bucket segment
         const uint64_t keep = l2_evict_last(), stream = l2_evict_first();
+        // parity of the last phase armed on each FULL barrier (-1: none), so
+        // that loads still in flight can be waited for on the way out
+        int armed_q[2] = {-1, -1}, armed_do[2] = {-1, -1}, armed_kv = -1;
         for (uint32_t j = 0;; ++j) {
           const uint32_t slot = j % kInfo;
           if (!wait_bar(sh, INFO_FULL + slot, (j / kInfo) & 1, a.status)) break;
@@ -297,6 +303,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
             tma_load_3d_hint(sm + OFF_K + 8192, &tmK, fb, 64, hi, e.kvrow, stream);
             tma_load_3d_hint(sm + OFF_V, &tmV, fb, 0, hi, e.kvrow, stream);
             tma_load_3d_hint(sm + OFF_V + 8192, &tmV, fb, 64, hi, e.kvrow, stream);
+            armed_kv = (int)(seg & 1);
           }
           const uint32_t qst = j & 1, qph = ((j >> 1) & 1) ^ 1;
           uint8_t* st = sm + OFF_QDO + qst * QDO_STAGE;
@@ -304,11 +311,22 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           mbar_arrive_expect_tx(&sh->bar[Q_FULL + qst], 32768u);
           tma_load_3d_hint(st, &tmQ, &sh->bar[Q_FULL + qst], 0, hi * 16, e.tok0, keep);
           tma_load_3d_hint(st + 16384, &tmQ, &sh->bar[Q_FULL + qst], 64, hi * 16, e.tok0, keep);
+          armed_q[qst] = (int)(qph ^ 1);
           if (!wait_bar(sh, DO_EMPTY + qst, qph, a.status)) break;
           mbar_arrive_expect_tx(&sh->bar[DO_FULL + qst], 32768u);
           tma_load_3d_hint(st + DO_IN_STAGE, &tmdO, &sh->bar[DO_FULL + qst], 0, hi * 16, e.tok0, keep);
           tma_load_3d_hint(st + DO_IN_STAGE + 16384, &tmdO, &sh->bar[DO_FULL + qst], 64, hi * 16, e.tok0, keep);
+          armed_do[qst] = (int)(qph ^ 1);
         }
+        // Every load issued has landed before the CTA can exit: after an abort
+        // some were never consumed.  One phase at most is pending per barrier
+        // (a barrier is re-armed only after its last phase was consumed), and
+        // on a normal exit each of these waits returns at once.
+        for (int s2 = 0; s2 < 2; ++s2) {
+          if (armed_q[s2] >= 0) wait_bar(sh, Q_FULL + s2, (uint32_t)armed_q[s2], a.status, false);
+          if (armed_do[s2] >= 0) wait_bar(sh, DO_FULL + s2, (uint32_t)armed_do[s2], a.status, false);
+        }
+        if (armed_kv >= 0) wait_bar(sh, KV_FULL, (uint32_t)armed_kv, a.status, false);
       }
     } else if (warp == kMmaWarp || warp == kMmaBWarp) {
       // ------------------------------------------------------------ MMA issuers

@@ -131,6 +131,8 @@ MSA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "mem
 // All but the most recent bulk group have finished reading their sources.
 MSA_DEV void bulk_wait_read_but_one() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 MSA_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Every bulk group of this thread has finished reading its source.
+MSA_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA engine, tensor core) before they read them.
 MSA_DEV void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
