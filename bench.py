@@ -19,7 +19,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -207,6 +206,7 @@ def _host_values(pb):
 # GPU leg
 # ---------------------------------------------------------------------------
 MAIN_KERNEL_SOURCES = ("msa_bwd.cu", "msa_bwd_ws.cuh", "msa_common.cuh")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "bwd_main_traffic.json")
 
 
 def kernel_source_sha1() -> str:
@@ -218,22 +218,55 @@ def kernel_source_sha1() -> str:
     return h.hexdigest()
 
 
-def _traffic_record(workload: str, tile: int):
-    """Per-launch DRAM bytes of the main kernel from the committed ncu summary,
-    valid only for the workload and query tiling it was captured on and while
-    the kernel source it was taken on is unchanged."""
-    sha = kernel_source_sha1()
-    path = os.path.join(ROOT, "profiles", "bwd_main_long128k.md")
-    if not os.path.exists(path):
-        return None
-    txt = open(path).read()
-    m = re.search(r"source_sha1:\s*([0-9a-f]{40})", txt)
-    t = re.search(r"traffic_bytes_per_launch_full:\s*([0-9.eE+]+)", txt)
-    w = re.search(r"workload:\s*(\S+)", txt)
-    c = re.search(r"task_tile_chunks:\s*(\d+)", txt)
-    if m and t and w and c and m.group(1) == sha and w.group(1) == workload and int(c.group(1)) == tile:
-        return float(t.group(1))
-    return None
+def traffic_record(workload: str, tile: int):
+    """(bytes per launch, note) of the main kernel's DRAM traffic from the
+    committed ncu record, or (None, why not).  The record holds counters taken
+    on a small case and scaled to the named workload by its task count; it is
+    valid only for that workload and tiling and while the kernel sources it was
+    taken on are unchanged."""
+    try:
+        with open(TRAFFIC_RECORD) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None, "no traffic record"
+    if rec.get("source_sha1") != kernel_source_sha1():
+        return None, "kernel changed since the ncu counters were taken"
+    scaled = rec.get("scaled", {}).get(f"{workload}/tile{tile}")
+    if scaled is None:
+        return None, f"no record scaled to {workload} with query tiles of {tile}"
+    return float(scaled["bytes_per_launch"]), scaled.get("how", "")
+
+
+def aux_bytes(pb, n_tasks: int) -> dict:
+    """Algorithmic (compulsory) DRAM bytes of each auxiliary stage per step."""
+    Hi, NC, K = pb.num_index_heads, pb.sel.shape[1], pb.topk
+    NB = int(sum(-(-int(n) // pb.block) for n in np.diff(pb.cu_seqlens)))
+    T, Hq, W, D = pb.total_tokens, pb.num_q_heads, pb.kv_rows, pb.head_dim
+    sizes = _chunk_sizes(pb)
+    edges = int(sum(int(np.count_nonzero(pb.sel[hi] >= 0, axis=1) @ sizes) for hi in range(Hi)))
+    sel_b, qi_b, rp_b = Hi * NC * K * 4, edges * 4, Hi * (NB + 1) * 4
+    return {
+        # sel read, row_ptr and q_indices written
+        "k2q": sel_b + qi_b + rp_b,
+        # row_ptr and q_indices read; task_meta (6), task_q_rows and task_q_pos (8 + 8) ints written per task
+        "tasks": rp_b + qi_b + n_tasks * (6 + 8 + 8) * 4,
+        # O, dO read; D written; dK/dV fp32 accumulators and the bf16 dQ output zeroed
+        "preprocess": 2 * T * Hq * D * 2 + T * Hq * 4 + 2 * W * Hi * D * 4 + T * Hq * D * 2,
+        # dK/dV fp32 accumulators read, bf16 dK/dV written
+        "postprocess": 2 * W * Hi * D * 4 + 2 * W * Hi * D * 2,
+    }
+
+
+def _chunk_sizes(pb) -> np.ndarray:
+    """Tokens of every query chunk, documents in order."""
+    out = []
+    for n in np.diff(pb.cu_seqlens):
+        n = int(n)
+        c = -(-n // pb.chunk)
+        sz = np.full(c, pb.chunk, np.int64)
+        sz[-1] = n - (c - 1) * pb.chunk
+        out.append(sz)
+    return np.concatenate(out)
 
 
 def run_gpu(args):
@@ -258,16 +291,17 @@ def run_gpu(args):
         raise B.MSAError(int(st[0].item()), "msa_fwd")
     flop = W.effective_flops(pb)
     stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
 
     # The forward (the next row on the path: it produces O and LSE) timed on its
     # own, outside the backward step: CUDA events around msa_fwd after one
     # warm-up call.  Effective FLOP count: QK^T and PV per selected block, 2/5
-    # of the backward's five GEMMs (the two-pass kernel computes QK^T twice).
+    # of the backward's five GEMMs.
     fwd_out = (torch.empty_like(o), torch.empty_like(lse), torch.zeros(4, dtype=torch.int32, device=dev))
     fwd_ws = torch.empty(max(256, 8 * (pb.num_docs + 1) + 256), dtype=torch.uint8, device=dev)
     fwd_runs = 3
     B.msa_fwd(prob, q, k, v, sel, *fwd_out[:2], fwd_out[2], fwd_ws)
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0, f1 = ev(), ev()
     f0.record(stream)
     for _ in range(fwd_runs):
         B.msa_fwd(prob, q, k, v, sel, *fwd_out[:2], fwd_out[2], fwd_ws)
@@ -280,17 +314,24 @@ def run_gpu(args):
     del fwd_out, fwd_ws
 
     bw = B.Backward(prob, task_tile_chunks=args.tile)
-    nsteps_events = []
+    STAGES = ("k2q", "tasks", "preprocess", "main", "postprocess")
 
-    def step(ev=None):
-        bw.build_tables(sel)
+    def step(evs=None):
+        """One pass of the hot path; evs (6 events) bracket its five stages on
+        the launching stream."""
+        rec = (lambda i: evs[i].record(stream)) if evs is not None else (lambda i: None)
+        rec(0)
+        B.msa_build_k2q(bw.p, sel, bw.row_ptr, bw.q_indices, bw.edge_cap, bw.status, bw.ws)
+        rec(1)
+        B.msa_build_tasks(bw.p, bw.row_ptr, bw.q_indices, bw.edge_cap, bw.tile, bw.task_meta, bw.task_q_rows,
+                          bw.task_q_pos, bw.walk, bw.task_cap, bw.num_sms, bw.status, bw.ws)
+        rec(2)
         bw.backward_stage(B.MSA_STAGE_PREPROCESS, q, k, v, o, do, lse)
-        if ev is not None:
-            ev[0].record(stream)
+        rec(3)
         bw.backward_stage(B.MSA_STAGE_MAIN, q, k, v, o, do, lse)
-        if ev is not None:
-            ev[1].record(stream)
+        rec(4)
         bw.backward_stage(B.MSA_STAGE_POSTPROCESS, q, k, v, o, do, lse)
+        rec(5)
 
     for _ in range(args.warmup):
         step()
@@ -298,9 +339,8 @@ def run_gpu(args):
     bw.check_status()
     n_tasks = bw.num_tasks()
 
-    main_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stage_ev = [[ev() for _ in range(6)] for _ in range(args.steps)]
+    t_start, t_end = ev(), ev()
     sampler = ClockSampler(local)
     if world > 1:
         dist.barrier()
@@ -309,7 +349,7 @@ def run_gpu(args):
     time.sleep(0.3)
     t_start.record(stream)
     for i in range(args.steps):
-        step(main_ev[i])
+        step(stage_ev[i])
     t_end.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -317,14 +357,18 @@ def run_gpu(args):
         dist.barrier()
     bw.check_status()
     ms = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, dev)
-    main_ms = sum(a.elapsed_time(b) for a, b in main_ev) / args.steps
+    stage_ms = {name: sum(e[i].elapsed_time(e[i + 1]) for e in stage_ev) / args.steps
+                for i, name in enumerate(STAGES)}
+    main_ms = stage_ms["main"]
     value = job_value(world, flop, ms)
 
     # End to end through the public API with host buffers (pinned), copies timed.
     # Each step copies its inputs host->device, runs the backward and reads dQ,
     # dK, dV back; the steps are pipelined over two device input/output sets
     # and three streams (H2D of step i+1 and D2H of step i-1 overlap step i's
-    # compute), as a serving loop would run them.
+    # compute), as a serving loop would run them.  Every copy batch is
+    # bracketed by events on its own stream, so the link rates below come from
+    # the same timed region as the end-to-end figure.
     pin = lambda t: t.cpu().pin_memory()
     host_in = {"q": pin(q), "k": pin(k), "v": pin(v), "o": pin(o), "do": pin(do), "lse": pin(lse), "sel": pin(sel)}
     host_out = [{n: torch.empty_like(getattr(bw, n), device="cpu").pin_memory() for n in ("dq", "dk", "dv")}
@@ -336,25 +380,27 @@ def run_gpu(args):
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
     s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev = lambda: torch.cuda.Event(enable_timing=True)
 
     def e2e_run(n_steps):
-        """Runs n_steps pipelined steps; returns (start, end) events."""
+        """Runs n_steps pipelined steps; returns (start, end, [(h2d start, end)], [(d2h start, end)])."""
         done = [None, None]      # compute of the last step that used set b finished
         out_free = [None, None]  # D2H of the last step that used set b finished
         start = ev()
         start.record(s_h2d)
-        end_events = []
+        end_events, h2d_ev, d2h_ev = [], [], []
         for i in range(n_steps):
             b = i % 2
             din, bwb = dev_in[b], bws[b]
             with torch.cuda.stream(s_h2d):
                 if done[b] is not None:
                     s_h2d.wait_event(done[b])
+                c0 = ev()
+                c0.record(s_h2d)
                 for name, t in host_in.items():
                     din[name].copy_(t, non_blocking=True)
                 ready = ev()
                 ready.record(s_h2d)
+                h2d_ev.append((c0, ready))
             stream.wait_event(ready)
             if out_free[b] is not None:
                 stream.wait_event(out_free[b])
@@ -363,41 +409,40 @@ def run_gpu(args):
             done[b].record(stream)
             with torch.cuda.stream(s_d2h):
                 s_d2h.wait_event(done[b])
+                c1 = ev()
+                c1.record(s_d2h)
                 for name in ("dq", "dk", "dv"):
                     host_out[b][name].copy_(getattr(bwb, name), non_blocking=True)
                 out_free[b] = ev()
                 out_free[b].record(s_d2h)
+                d2h_ev.append((c1, out_free[b]))
             end_events.append(out_free[b])
-        return start, end_events[-1]
-
-    def copy_rate(fn, stream_):
-        a, b_ = ev(), ev()
-        a.record(stream_)
-        with torch.cuda.stream(stream_):
-            fn()
-        b_.record(stream_)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b_)
+        return start, end_events[-1], h2d_ev, d2h_ev
 
     e2e_steps = max(2, min(args.steps, 6))
     e2e_run(2)
     torch.cuda.synchronize()
-    h2d_ms = copy_rate(lambda: [dev_in[1][n].copy_(t, non_blocking=True) for n, t in host_in.items()], s_h2d)
-    d2h_ms = copy_rate(lambda: [host_out[1][n].copy_(getattr(bws[1], n), non_blocking=True)
-                                for n in ("dq", "dk", "dv")], s_d2h)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    e0, e1 = e2e_run(e2e_steps)
+    e0, e1, h2d_ev, d2h_ev = e2e_run(e2e_steps)
     torch.cuda.synchronize()
     for b_ in bws:
         b_.check_status()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
     e2e_value = job_value(world, flop, e2e_ms)
+    h2d_ms = sum(a_.elapsed_time(b_) for a_, b_ in h2d_ev)
+    d2h_ms = sum(a_.elapsed_time(b_) for a_, b_ in d2h_ev)
 
     burst, sustained, hbm, src = _peaks()
     achieved = flop / (main_ms * 1e-3) / 1e12
-    traffic = _traffic_record(args.workload, args.tile)
+    traffic, traffic_note = traffic_record(args.workload, args.tile)
+    abytes = aux_bytes(pb, n_tasks)
+    aux = {name: {"ms": stage_ms[name], "algorithmic_bytes": abytes[name],
+                  "gbs": abytes[name] / (stage_ms[name] * 1e-3) / 1e9,
+                  "frac_of_hbm": abytes[name] / (stage_ms[name] * 1e-3) / 1e9 / hbm}
+           for name in ("k2q", "tasks", "preprocess", "postprocess")}
+    n_launches = 5 + 6 + 3 + 1 + 1  # CSR build, task build, preprocess, counter reset + main, postprocess
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -407,20 +452,28 @@ def run_gpu(args):
                    "block": pb.block, "chunk": pb.chunk, "topk": pb.topk, "tasks": n_tasks,
                    "effective_tflop_per_step": flop / 1e12, "task_tile_chunks": args.tile,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
-        "fraction_of_peak": {"value": value / sustained, "peak_tflops": sustained,
-                             "peak_kind": f"bf16 sustained ({src})"},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
-                     "frac": achieved / sustained, "traffic": traffic, "kernel": "bwd_main",
-                     "kernel_ms": main_ms, "peak_kind": f"bf16 sustained, of {src}"},
+        "fraction_of_peak": {"value": value / burst, "peak_tflops": burst, "peak_kind": f"bf16 burst ({src})",
+                             "value_vs_sustained": value / sustained, "sustained_tflops": sustained},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
+                     "frac": achieved / burst, "traffic": traffic, "kernel": "bwd_main_ws",
+                     "kernel_ms": main_ms, "peak_kind": f"bf16 burst, of {src}",
+                     "frac_vs_sustained": achieved / sustained, "sustained_peak": sustained,
+                     "traffic_note": traffic_note},
+        "stages_ms": stage_ms,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "steps": e2e_steps,
                 "pipeline": "H2D of step i+1 and D2H of step i-1 overlap step i (two device sets, three streams)",
-                "h2d_gbs": h2d / (h2d_ms * 1e-3) / 1e9, "d2h_gbs": d2h / (d2h_ms * 1e-3) / 1e9},
-        "gpu_launches": args.steps * 14,
+                "h2d_gbs": h2d * e2e_steps / (h2d_ms * 1e-3) / 1e9,
+                "d2h_gbs": d2h * e2e_steps / (d2h_ms * 1e-3) / 1e9,
+                "h2d_ms_per_step": h2d_ms / e2e_steps, "d2h_ms_per_step": d2h_ms / e2e_steps,
+                "copy_timing": "per-step events on the copy streams inside the timed region"},
+        "gpu_launches": args.steps * n_launches,
         "next_rows": {"forward": {"kernel_ms": fwd_ms, "effective_tflops": fwd_flop / (fwd_ms * 1e-3) / 1e12,
-                                  "frac": fwd_flop / (fwd_ms * 1e-3) / 1e12 / sustained,
+                                  "frac": fwd_flop / (fwd_ms * 1e-3) / 1e12 / burst,
+                                  "frac_vs_sustained": fwd_flop / (fwd_ms * 1e-3) / 1e12 / sustained,
                                   "flop_convention": "QK^T and PV per selected block (2 of the 5 backward GEMMs)",
-                                  "timed": "3 msa_fwd calls after one warm-up, outside the backward step"}},
+                                  "timed": "3 msa_fwd calls after one warm-up, outside the backward step"},
+                      "aux_kernels": aux},
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

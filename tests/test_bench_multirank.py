@@ -65,10 +65,21 @@ def test_ranks_draw_independent_batches():
     assert not np.array_equal(a.sel, b.sel)
 
 
-def test_traffic_record_applies_only_to_its_workload_and_tiling():
+def test_traffic_record_applies_only_to_its_workload_and_tiling(tmp_path, monkeypatch):
     sys.path.insert(0, ROOT)
     import bench
-    rec = bench._traffic_record("long128k", 1024)
-    assert rec is None or rec > 0          # None once the kernel sources changed since the capture
-    assert bench._traffic_record("single8k", 0) is None
-    assert bench._traffic_record("long128k", 512) is None
+    import json
+    rec_path = tmp_path / "traffic.json"
+    rec = {"source_sha1": bench.kernel_source_sha1(),
+           "scaled": {"long128k/tile1024": {"bytes_per_launch": 2.5e10, "how": "test"}}}
+    rec_path.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_RECORD", str(rec_path))
+    assert bench.traffic_record("long128k", 1024)[0] == 2.5e10
+    assert bench.traffic_record("single8k", 0)[0] is None
+    assert bench.traffic_record("long128k", 512)[0] is None
+    rec["source_sha1"] = "0" * 40                      # counters of another build of the kernel
+    rec_path.write_text(json.dumps(rec))
+    value, why = bench.traffic_record("long128k", 1024)
+    assert value is None and "changed" in why
+    monkeypatch.setattr(bench, "TRAFFIC_RECORD", str(tmp_path / "missing.json"))
+    assert bench.traffic_record("long128k", 1024)[0] is None
