@@ -237,6 +237,23 @@ def traffic_record(workload: str, tile: int):
     return float(scaled["bytes_per_launch"]), scaled.get("how", "")
 
 
+# fp32 FMA issue peak of the GPU: 152 SMs x 128 FMA lanes x 2 FLOP x 2.07 GHz.
+FP32_FMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def scorer_flops(pb) -> int:
+    """Score FLOPs of the block scorer: one 128-dim dot product (2 x 128 FLOP)
+    per index head, query chunk and key block strictly before the chunk's
+    diagonal block (the diagonal is selected without a score)."""
+    cu = np.asarray(pb.cu_seqlens, dtype=np.int64)
+    pairs = 0
+    for d in range(len(cu) - 1):
+        n = int(cu[d + 1] - cu[d])
+        c = np.arange((n + pb.chunk - 1) // pb.chunk, dtype=np.int64)
+        pairs += int(((c * pb.chunk) // pb.block).sum())
+    return pairs * pb.num_index_heads * 2 * 128
+
+
 def aux_bytes(pb, n_tasks: int) -> dict:
     """Algorithmic (compulsory) DRAM bytes of each auxiliary stage per step."""
     Hi, NC, K = pb.num_index_heads, pb.sel.shape[1], pb.topk
@@ -311,7 +328,43 @@ def run_gpu(args):
         raise B.MSAError(int(fwd_out[2][0].item()), "msa_fwd")
     fwd_ms = f0.elapsed_time(f1) / fwd_runs
     fwd_flop = flop * 2 / 5
-    del fwd_out, fwd_ws
+
+    # The planner and the forward walking its plan, timed the same way.
+    plan_meta, plan_wc, plan_st = B.plan_forward(prob, sel)
+    plan_ws = torch.empty(B.msa_workspace_bytes(prob, 1, 1, 0), dtype=torch.uint8, device=dev)
+    B.msa_fwd_planned(prob, q, k, v, sel, plan_meta, *fwd_out[:2], fwd_out[2], fwd_ws)
+    f0.record(stream)
+    for _ in range(fwd_runs):
+        B.msa_plan_forward(prob, sel, plan_meta, plan_wc, plan_st, plan_ws)
+    f1.record(stream)
+    f2 = ev()
+    for _ in range(fwd_runs):
+        B.msa_fwd_planned(prob, q, k, v, sel, plan_meta, *fwd_out[:2], fwd_out[2], fwd_ws)
+    f2.record(stream)
+    torch.cuda.synchronize()
+    for t, what in ((plan_st, "msa_plan_forward"), (fwd_out[2], "msa_fwd_planned")):
+        if int(t[0].item()) != 0:
+            raise B.MSAError(int(t[0].item()), what)
+    plan_ms = f0.elapsed_time(f1) / fwd_runs
+    fwd_planned_ms = f1.elapsed_time(f2) / fwd_runs
+    del fwd_out, fwd_ws, plan_meta, plan_wc, plan_st, plan_ws
+
+    # The block scorer + top-k on seeded index projections of the same shape.
+    qi_idx, ki_idx = W.device_index_values(pb, dev, seed=rank)
+    sel_scored = torch.empty_like(sel)
+    sc_st = torch.zeros(4, dtype=torch.int32, device=dev)
+    sc_ws = torch.empty(B.msa_workspace_bytes(prob, 1, 1, 0), dtype=torch.uint8, device=dev)
+    B.msa_select_topk(prob, qi_idx, ki_idx, sel_scored, sc_st, sc_ws)
+    f0.record(stream)
+    for _ in range(fwd_runs):
+        B.msa_select_topk(prob, qi_idx, ki_idx, sel_scored, sc_st, sc_ws)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    if int(sc_st[0].item()) != 0:
+        raise B.MSAError(int(sc_st[0].item()), "msa_select_topk")
+    score_ms = f0.elapsed_time(f1) / fwd_runs
+    score_flop = scorer_flops(pb)
+    del qi_idx, ki_idx, sel_scored, sc_st, sc_ws
 
     bw = B.Backward(prob, task_tile_chunks=args.tile)
     STAGES = ("k2q", "tasks", "preprocess", "main", "postprocess")
@@ -473,6 +526,15 @@ def run_gpu(args):
                                   "frac_vs_sustained": fwd_flop / (fwd_ms * 1e-3) / 1e12 / sustained,
                                   "flop_convention": "QK^T and PV per selected block (2 of the 5 backward GEMMs)",
                                   "timed": "3 msa_fwd calls after one warm-up, outside the backward step"},
+                      "forward_planned": {"plan_ms": plan_ms, "kernel_ms": fwd_planned_ms,
+                                          "effective_tflops": fwd_flop / (fwd_planned_ms * 1e-3) / 1e12,
+                                          "timed": "3 msa_plan_forward then 3 msa_fwd_planned calls after "
+                                                   "one warm-up"},
+                      "scorer": {"ms": score_ms, "score_gflop": score_flop / 1e9,
+                                 "score_tflops": score_flop / (score_ms * 1e-3) / 1e12,
+                                 "bound": "alu", "fp32_fma_peak_tflops": FP32_FMA_PEAK_TFLOPS,
+                                 "frac": score_flop / (score_ms * 1e-3) / 1e12 / FP32_FMA_PEAK_TFLOPS,
+                                 "timed": "3 msa_select_topk calls on seeded index projections after one warm-up"},
                       "aux_kernels": aux},
         "clocks": clocks,
     }

@@ -49,6 +49,9 @@ WORKLOADS = {
                       policy="diag_uniform"),
     "long128k": dict(lengths=[131072], num_index_heads=8, topk=32, policy="diag_recent3_uniform"),
     "zipf64k": dict(lengths=[8192] * 8, num_index_heads=4, topk=16, policy="zipf", zipf_s=1.2),
+    # one index head of long128k (an eighth of its tasks, same causal and
+    # per-tile structure): the small case for hardware-counter captures
+    "long128k_1head": dict(lengths=[131072], num_index_heads=1, topk=32, policy="diag_recent3_uniform"),
 }
 
 
