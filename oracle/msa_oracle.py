@@ -555,7 +555,7 @@ def build_k2q(sel, cu_seqlens, block, chunk, validate=True):
     return row_ptr.astype(np.int32), q_indices.astype(np.int32)
 
 
-def build_tasks(row_ptr, q_indices, cu_seqlens, block, chunk, tile_chunks=0):
+def build_tasks(row_ptr, q_indices, cu_seqlens, block, chunk, tile_chunks=0, key_tile=64):
     """Task rows of the KV-parallel backward.
 
     Each CSR row's entries are cut into consecutive groups of ``chunk``
@@ -565,12 +565,25 @@ def build_tasks(row_ptr, q_indices, cu_seqlens, block, chunk, tile_chunks=0):
     query // tile_chunks; a single tile when tile_chunks is 0), then key-block
     row, then CSR offset.
 
+    Key tiles (not in the pages; the kernel's tile is 64 keys): a block wider
+    than ``key_tile`` keys is cut into block // key_tile tiles, and a group
+    becomes one task per tile whose first key is at or before the group's last
+    query (the tiles after it would be fully masked).  Row r, tile h is task
+    row r * (block // key_tile) + h and its document-local kblock is counted
+    in key tiles (b * (block // key_tile) + h); the order is (index head,
+    query tile, that task row, CSR offset).  Blocks of at most ``key_tile``
+    keys are one tile, so the rows and kblocks are the CSR's.
+
     Returns task_meta int32 [n, 6] with columns (index_head, row_linear,
     q_begin, q_count, document_ordinal, document_local_kblock), q_begin being
     the CSR offset of the task's first entry; task_q_rows int32 [n, C]
     (compact token row, -1 pad) and task_q_pos int32 [n, C] (document-local
     position, -1 pad).
     """
+    nh = 1
+    if block > key_tile:
+        assert block % key_tile == 0, "a block must be a whole number of key tiles"
+        nh = block // key_tile
     lay = DocLayout(cu_seqlens, block, chunk)
     row_ptr = np.asarray(row_ptr, dtype=np.int64)
     q_indices = np.asarray(q_indices, dtype=np.int64)
@@ -590,7 +603,11 @@ def build_tasks(row_ptr, q_indices, cu_seqlens, block, chunk, tile_chunks=0):
         b = r - lay.blk_off[d]
         g = lay.chunk_off[d] + q_indices[hi, starts] // chunk
         tile = g // tile_chunks if tile_chunks > 0 else np.zeros_like(g)
-        cols.append((np.full(starts.size, hi), tile, r, starts, cnt, d, b))
+        last = q_indices[hi, starts + cnt - 1]                # the group's last query
+        for h in range(nh):
+            reach = b * block + h * key_tile <= last
+            cols.append((np.full(int(reach.sum()), hi), tile[reach], r[reach] * nh + h, starts[reach],
+                         cnt[reach], d[reach], b[reach] * nh + h))
     hi_, tile, r, starts, cnt, d, b = (np.concatenate(c) for c in zip(*cols))
     order = np.lexsort((starts, r, tile, hi_))
     hi_, r, starts, cnt, d, b = (a[order] for a in (hi_, r, starts, cnt, d, b))

@@ -173,3 +173,40 @@ def test_forward_plan_orders_longest_first_and_counts_nonempty_items():
         assert q_begin == lay.cu[d] + c * pb.chunk
         assert q_count == min(pb.chunk, lay.lengths[d] - c * pb.chunk)
         assert kb == c * pb.chunk // pb.block
+
+
+@pytest.mark.parametrize("block,key_tile", [(32, 16), (128, 64)])
+def test_key_tiles_cover_every_attended_pair_once(block, key_tile):
+    # Blocks wider than the kernel's key tile become one task per reached tile:
+    # brute force over (head, document, query, key) pairs that the selection
+    # and the causal mask admit, each in exactly one task, and no task whose
+    # tile no query of the group reaches.
+    lengths = [300, 129, 64] if block == 128 else [100, 33, 70]
+    pb = W.make_problem(lengths=lengths, num_index_heads=2, topk=3, policy="diag_uniform", seed=4,
+                        values=False, block=block, chunk=8)
+    lay = O.DocLayout(pb.cu_seqlens, block, 8)
+    rp, qi = O.build_k2q(pb.sel, pb.cu_seqlens, block, 8)
+    tile_chunks = 2
+    m, qr, qp = O.build_tasks(rp, qi, pb.cu_seqlens, block, 8, tile_chunks=tile_chunks, key_tile=key_tile)
+    nh = block // key_tile
+    want = set()
+    for hi in range(2):
+        for d in range(lay.num_docs):
+            n = int(lay.lengths[d])
+            for p in range(n):
+                for b in pb.sel[hi, lay.chunk_off[d] + p // 8]:
+                    if b >= 0:
+                        want.update((hi, d, p, key) for key in range(b * block, min((b + 1) * block, p + 1)))
+    got, order = [], []
+    for t in range(m.shape[0]):
+        hi, rt, s, cnt, d, kb = (int(x) for x in m[t])
+        assert rt == (int(lay.blk_off[d]) + kb // nh) * nh + kb % nh
+        n = int(lay.lengths[d])
+        pairs = [(hi, d, int(p), key) for p in qp[t, :cnt]
+                 for key in range(kb * key_tile, min((kb + 1) * key_tile, n)) if key <= p]
+        assert pairs, "a task whose key tile no query of the group reaches"
+        got.extend(pairs)
+        order.append((hi, (int(lay.chunk_off[d]) + int(qp[t, 0]) // 8) // tile_chunks, rt, s))
+    assert len(got) == len(set(got))
+    assert set(got) == want
+    assert order == sorted(order)
