@@ -29,6 +29,7 @@ MSA_ERR_SCRATCH_TOO_SMALL = 9
 MSA_NOALLOC_SCRATCH_BYTES = 16 << 20
 MSA_TASK_META_COLS = 6
 MSA_STAGE_PREPROCESS, MSA_STAGE_MAIN, MSA_STAGE_POSTPROCESS, MSA_STAGE_ALL = 1, 2, 4, 7
+MSA_BWD_DQ_FP32 = 8
 MSA_WALK_LEN = 8
 
 HEAD_DIM, BLOCK, CHUNK, GROUP = 128, 64, 8, 16
@@ -69,6 +70,7 @@ def _load():
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     sig = {
         "msa_workspace_bytes": (sz, [P, i64, i64, i32]),
+        "msa_workspace_bytes_opts": (sz, [P, i64, i64, i32, ctypes.c_uint32]),
         "msa_build_k2q": (ctypes.c_int, [P, vp, vp, vp, i64, vp, vp, sz, vp]),
         "msa_build_k2q_noalloc": (ctypes.c_int, [P, vp, vp, vp, i64, vp, vp]),
         "msa_build_tasks": (ctypes.c_int, [P, vp, vp, i64, i32, vp, vp, vp, vp, i64, i32, vp, vp, sz, vp]),
@@ -168,6 +170,7 @@ class Problem:
     softmax_scale: float
     d_cu: object = None
     d_kvs: object = None
+    block_size: int = BLOCK   # keys per selectable block: 64, or 128 (two 64-key tiles)
 
     @property
     def num_docs(self):
@@ -187,7 +190,7 @@ class Problem:
 
     @property
     def num_blocks(self):
-        return int(sum(-(-n // BLOCK) for n in self.lengths))
+        return int(sum(-(-n // self.block_size) for n in self.lengths))
 
     @property
     def num_chunks(self):
@@ -195,11 +198,11 @@ class Problem:
 
     def edge_capacity(self) -> int:
         """Upper bound on CSR entries per index head: every chunk selects topk blocks."""
-        return max(1, int(sum(min(self.topk, -(-int(n) // BLOCK)) * int(n) for n in self.lengths)))
+        return max(1, int(sum(min(self.topk, -(-int(n) // self.block_size)) * int(n) for n in self.lengths)))
 
     def task_capacity(self) -> int:
-        """Upper bound on task rows: one per valid selection slot."""
-        return max(1, self.num_index_heads * self.num_chunks * self.topk)
+        """Upper bound on task rows: one per valid selection slot and 64-key tile."""
+        return max(1, self.num_index_heads * self.num_chunks * self.topk * max(1, self.block_size // BLOCK))
 
     def c_struct(self) -> msa_problem:
         s = msa_problem()
@@ -212,7 +215,7 @@ class Problem:
         s.num_index_heads = self.num_index_heads
         s.num_kv_heads = self.num_index_heads
         s.head_dim = HEAD_DIM
-        s.block_size = BLOCK
+        s.block_size = int(self.block_size)
         s.query_chunk = CHUNK
         s.topk = int(self.topk)
         s.num_blocks = self.num_blocks
@@ -222,11 +225,11 @@ class Problem:
 
 
 def make_problem(cu_seqlens, kv_doc_starts, kv_rows, num_q_heads, topk, softmax_scale=HEAD_DIM ** -0.5,
-                 device="cuda") -> Problem:
+                 device="cuda", block_size=BLOCK) -> Problem:
     import torch
     cu = np.asarray(cu_seqlens, np.int32)
     kvs = np.asarray(kv_doc_starts, np.int32)
-    p = Problem(cu, kvs, int(kv_rows), int(num_q_heads), int(topk), float(softmax_scale))
+    p = Problem(cu, kvs, int(kv_rows), int(num_q_heads), int(topk), float(softmax_scale), block_size=int(block_size))
     p.d_cu = torch.tensor(cu, dtype=torch.int32, device=device)
     p.d_kvs = torch.tensor(kvs, dtype=torch.int32, device=device)
     return p
@@ -239,6 +242,13 @@ def make_problem(cu_seqlens, kv_doc_starts, kv_rows, num_q_heads, topk, softmax_
 def msa_workspace_bytes(p: Problem, edge_cap: int, task_cap: int, task_tile_chunks: int = 0) -> int:
     s = p.c_struct() if p.d_cu is not None else None
     return int(lib.msa_workspace_bytes(ctypes.byref(s), int(edge_cap), int(task_cap), int(task_tile_chunks)))
+
+
+def msa_workspace_bytes_opts(p: Problem, edge_cap: int, task_cap: int, task_tile_chunks: int = 0,
+                             options: int = 0) -> int:
+    s = p.c_struct() if p.d_cu is not None else None
+    return int(lib.msa_workspace_bytes_opts(ctypes.byref(s), int(edge_cap), int(task_cap), int(task_tile_chunks),
+                                            int(options)))
 
 
 def msa_build_k2q(p: Problem, sel, row_ptr, q_indices, edge_cap, d_status, ws, stream=None):
@@ -351,7 +361,8 @@ class Backward:
     msa_bwd on the current stream and returns bf16 (dq, dk, dv) tensors.
     """
 
-    def __init__(self, p: Problem, task_tile_chunks: int = 0, num_sms: int = 0, edge_cap=None, task_cap=None):
+    def __init__(self, p: Problem, task_tile_chunks: int = 0, num_sms: int = 0, edge_cap=None, task_cap=None,
+                 dq_fp32: bool = False):
         import torch
         self.p = p
         dev = p.d_cu.device
@@ -368,7 +379,8 @@ class Backward:
         self.task_q_pos = torch.empty((self.task_cap, CHUNK), dtype=i32, device=dev)
         self.walk = torch.zeros(MSA_WALK_LEN, dtype=i32, device=dev)
         self.status = torch.zeros(4, dtype=i32, device=dev)
-        nbytes = msa_workspace_bytes(p, self.edge_cap, self.task_cap, self.tile)
+        self.options = MSA_BWD_DQ_FP32 if dq_fp32 else 0
+        nbytes = msa_workspace_bytes_opts(p, self.edge_cap, self.task_cap, self.tile, self.options)
         if nbytes == 0:
             raise MSAError(MSA_ERR_INVALID_ARGUMENT, "msa_workspace_bytes")
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
@@ -385,13 +397,17 @@ class Backward:
                         self.ws, stream)
 
     def backward(self, q, k, v, o, do, lse, stream=None):
-        msa_bwd(self.p, q, k, v, o, do, lse, self.task_meta, self.task_q_rows, self.task_q_pos, self.walk,
-                self.task_cap, self.dq, self.dk, self.dv, self.status, self.ws, stream)
+        if self.options:
+            self.backward_stage(MSA_STAGE_ALL, q, k, v, o, do, lse, stream)
+        else:
+            msa_bwd(self.p, q, k, v, o, do, lse, self.task_meta, self.task_q_rows, self.task_q_pos, self.walk,
+                    self.task_cap, self.dq, self.dk, self.dv, self.status, self.ws, stream)
         return self.dq, self.dk, self.dv
 
     def backward_stage(self, stages, q, k, v, o, do, lse, stream=None):
         msa_bwd_staged(self.p, q, k, v, o, do, lse, self.task_meta, self.task_q_rows, self.task_q_pos, self.walk,
-                       self.task_cap, self.dq, self.dk, self.dv, self.status, self.ws, stages, stream)
+                       self.task_cap, self.dq, self.dk, self.dv, self.status, self.ws, stages | self.options,
+                       stream)
 
     def run(self, sel, q, k, v, o, do, lse, stream=None):
         self.build_tables(sel, stream)

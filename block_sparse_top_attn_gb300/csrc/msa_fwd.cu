@@ -34,12 +34,13 @@ constexpr uint32_t OFF_Q = 0;       // [2 halves][128 rows][128 B]
 constexpr uint32_t OFF_K = 32768;   // 2 buffers x [2 halves][64 keys][128 B]
 constexpr uint32_t OFF_V = 65536;   // 2 buffers x [2 halves][64 keys][128 B]
 constexpr uint32_t OFF_BAR = 98304;
-constexpr uint32_t BAR_BYTES = 256;
+constexpr uint32_t BAR_BYTES = 512;  // barriers, TMEM slot, the item's key-tile list
 // Slack for aligning the dynamic window to 1024 B.  A window that would need
 // more than this is reported.
 constexpr uint32_t ALIGN_SLACK = 768;
 constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + ALIGN_SLACK;
 constexpr uint32_t TMEM_COLS = 256;
+constexpr int kMaxTiles = 64;  // 64-key tiles of an item: up to 32 blocks of 128 keys
 constexpr uint32_t COL_S = 0, COL_P = 64, COL_O = 128;  // S 64 columns, P 2 x 32 (bf16 pairs), O 128
 constexpr float kTau = 8.f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -92,6 +93,7 @@ struct FwdArgs {
   uint16_t* o;
   float* lse;
   int N, NC, K, Hi, Hq;
+  int nh;  // 64-key tiles per selected block (1 or 2)
   float scale_log2;
   int32_t* status;
 };
@@ -136,7 +138,8 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
   // issuer's wait independent of that ordering.
   uint64_t* bar_pfull = bar_q + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 11);
-  int* s_blocks = reinterpret_cast<int*>(bar_q + 12);  // up to 32 selected blocks, count at [32]
+  // the item's 64-key tiles (up to 2 per selected block), count at [kMaxTiles]
+  int* s_blocks = reinterpret_cast<int*>(bar_q + 12);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     mbar_init(bar_q, 1);
@@ -174,14 +177,32 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
     const int hi = a.plan ? a.plan[w * MSA_TASK_META_COLS] : (int)(w / a.NC);
     const int g = a.plan ? a.plan[w * MSA_TASK_META_COLS + 1] : (int)(w % a.NC);
     const int d = doc_of_chunk(a.chunk_off, a.N + 1, g);
-    if (warp == kIssueWarp) {  // compact the item's selection, order kept
+    if (warp == kIssueWarp) {
+      // compact the item's selection into 64-key tiles, order kept: a 128-key
+      // block gives its lower tile and, when the chunk's last query reaches
+      // it, its upper tile
       const int b = lane < a.K ? a.sel[((int64_t)hi * a.NC + g) * a.K + lane] : -1;
-      const uint32_t m = __ballot_sync(0xffffffffu, b >= 0);
-      if (b >= 0) s_blocks[__popc(m & ((1u << lane) - 1u))] = b;
-      if (lane == 0) s_blocks[32] = __popc(m);
+      int ntl = 0;
+      if (b >= 0) {
+        ntl = 1;
+        if (a.nh > 1) {
+          const int c = g - a.chunk_off[d];
+          const int last = min(c * 8 + 7, a.cu[d + 1] - a.cu[d] - 1);
+          ntl = (b * 128 + 64 <= last) ? 2 : 1;
+        }
+      }
+      int x = ntl;
+#pragma unroll
+      for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o2);
+        if (lane >= o2) x += y;
+      }
+      const int at = x - ntl;
+      for (int i = 0; i < ntl; ++i) s_blocks[at + i] = b * a.nh + i;
+      if (lane == 31) s_blocks[fwd::kMaxTiles] = x;
     }
     if (__syncthreads_or(aborted)) break;
-    const int nblk = s_blocks[32];
+    const int nblk = s_blocks[fwd::kMaxTiles];
     const int kv0 = kv_doc_starts[d];
     const uint32_t seq0 = seq;
     if (warp == kIssueWarp) {
@@ -419,7 +440,7 @@ __global__ void __launch_bounds__(fwd::kThreads, 1)
 }
 
 // defined in msa_tables.cu
-__global__ void layout_kernel(const int32_t* cu, const int32_t* kvs, int N, int T, int W, int NB, int NC,
+__global__ void layout_kernel(const int32_t* cu, const int32_t* kvs, int N, int T, int W, int B, int NB, int NC,
                               int32_t* blk_off, int32_t* chunk_off, int32_t* status);
 
 }  // namespace msa
@@ -449,7 +470,7 @@ static int launch_fwd(const msa_problem* p, const uint16_t* q, const uint16_t* k
         make_tmap_3d(&tmV, v, false, W, Hkv, 64, 1, 64)))
     return MSA_ERR_CUDA;
   layout_kernel<<<1, 1024, 0, st>>>(p->cu_seqlens, p->kv_doc_starts, N, p->total_tokens, p->kv_rows,
-                                    p->num_blocks, p->num_chunks, blk_off, chunk_off, d_status);
+                                    p->block_size, p->num_blocks, p->num_chunks, blk_off, chunk_off, d_status);
   // The largest shared-memory carveout: two CTAs of ~97 KB share one SM.
   if (cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fwd::SMEM) != cudaSuccess ||
       cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -457,7 +478,7 @@ static int launch_fwd(const msa_problem* p, const uint16_t* q, const uint16_t* k
     return MSA_ERR_CUDA;
   FwdArgs a;
   a.sel = sel; a.plan = plan; a.cu = p->cu_seqlens; a.chunk_off = chunk_off; a.o = o; a.lse = lse; a.N = N;
-  a.NC = p->num_chunks; a.K = p->topk; a.Hi = p->num_index_heads; a.Hq = (int)Hq;
+  a.NC = p->num_chunks; a.K = p->topk; a.Hi = p->num_index_heads; a.Hq = (int)Hq; a.nh = key_tiles_per_block(p);
   a.scale_log2 = p->softmax_scale * fwd::kLog2e; a.status = d_status;
   const int64_t items = (int64_t)p->num_index_heads * p->num_chunks;
   // CTAs resident per SM: shared memory per SM over this CTA's share (with

@@ -90,7 +90,7 @@ struct TopkArgs {
   const int32_t* chunk_off;
   const int32_t* blk_off;
   int32_t* sel;            // [Hi, NC, K]
-  int N, Hi, NC, NB, K;
+  int N, Hi, NC, NB, K, B;
   int32_t* status;
 };
 
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     int lo = 0, n = -1;
     if (g < a.NC) {
       const int d = doc_of(a.chunk_off, a.N + 1, g);
-      const int diag = ((g - a.chunk_off[d]) * kChunk) / kBlock;
+      const int diag = ((g - a.chunk_off[d]) * kChunk) / a.B;
       lo = a.blk_off[d];
       n = diag;
     }
@@ -251,9 +251,9 @@ extern "C" int msa_select_topk(const msa_problem* p, const uint16_t* q_index, co
   if ((rc = sm_count_current(&sms))) return rc;
   score::PoolArgs pa{q_index, qpool, p->cu_seqlens, chunk_off, N, Hi, NC, kChunk, d_status};
   score::pool_kernel<<<sms * 8, 256, 0, st>>>(pa);
-  score::PoolArgs pk{k_index, kpool, p->cu_seqlens, blk_off, N, Hi, NB, kBlock, d_status};
+  score::PoolArgs pk{k_index, kpool, p->cu_seqlens, blk_off, N, Hi, NB, p->block_size, d_status};
   score::pool_kernel<<<sms * 8, 256, 0, st>>>(pk);
-  score::TopkArgs ta{qpool, kpool, chunk_off, blk_off, sel, N, Hi, NC, NB, p->topk, d_status};
+  score::TopkArgs ta{qpool, kpool, chunk_off, blk_off, sel, N, Hi, NC, NB, p->topk, p->block_size, d_status};
   if ((rc = cuda_status(cudaFuncSetAttribute(score::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)score::SMEM))))
     return rc;

@@ -52,6 +52,9 @@ WORKLOADS = {
     # one index head of long128k (an eighth of its tasks, same causal and
     # per-tile structure): the small case for hardware-counter captures
     "long128k_1head": dict(lengths=[131072], num_index_heads=1, topk=32, policy="diag_recent3_uniform"),
+    # 128-key blocks: the same keys per chunk (16 x 128 = 32 x 64)
+    "single8k_b128": dict(lengths=[8192], num_index_heads=4, topk=8, policy="diag_uniform", block=128),
+    "long128k_b128": dict(lengths=[131072], num_index_heads=8, topk=16, policy="diag_recent3_uniform", block=128),
 }
 
 
@@ -197,6 +200,7 @@ def make_problem(name: str | None = None, *, seed: int = 0, lengths=None,
         topk = spec["topk"]
         policy = spec["policy"]
         zipf_s = spec.get("zipf_s", zipf_s)
+        block = spec.get("block", block)
     lengths = [int(n) for n in lengths]
     sel = draw_selection(rng, lengths, num_index_heads, topk, policy, block, chunk, zipf_s)
     cu = np.zeros(len(lengths) + 1, dtype=np.int32)

@@ -30,7 +30,7 @@ def upload(pb, device="cuda"):
     import torch
     from block_sparse_top_attn_gb300 import binding as B
     prob = B.make_problem(pb.cu_seqlens, pb.kv_doc_starts, pb.kv_rows, pb.num_q_heads, pb.topk,
-                          pb.softmax_scale, device=device)
+                          pb.softmax_scale, device=device, block_size=pb.block)
     t = {"sel": torch.from_numpy(np.ascontiguousarray(pb.sel)).to(device)}
     if pb.q is not None:
         for name in ("q", "k", "v", "do"):

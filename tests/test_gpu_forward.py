@@ -18,12 +18,15 @@ def B():
     return binding
 
 
-@pytest.mark.parametrize("case", ["tiny", "ragged", "single8k"])
+@pytest.mark.parametrize("case", ["tiny", "ragged", "single8k", "single8k_b128", "ragged_block128"])
 def test_forward_matches_oracle(B, case):
     import torch
     if case == "ragged":
         pb = W.make_problem(lengths=[200, 77, 1, 130, 9], num_index_heads=2, topk=4, policy="diag_uniform",
                             kv_layout="aligned", seed=3)
+    elif case == "ragged_block128":
+        pb = W.make_problem(lengths=[65, 127, 1, 129, 300, 9], num_index_heads=2, topk=3, policy="diag_uniform",
+                            kv_layout="aligned", seed=13, block=128)
     else:
         pb = W.make_problem(case)
     prob, t = upload(pb)

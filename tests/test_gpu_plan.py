@@ -37,7 +37,8 @@ def _case(name):
     return pb
 
 
-@pytest.mark.parametrize("name", ["tiny", "single8k", "varlen32k", "zipf64k", "long128k", "ragged_empty"])
+@pytest.mark.parametrize("name", ["tiny", "single8k", "varlen32k", "zipf64k", "long128k", "ragged_empty",
+                                  "single8k_b128"])
 def test_plan_bit_exact(B, name):
     import torch
     pb = _case(name)

@@ -34,13 +34,16 @@ def _gpu_sel(B, pb, qi, ki):
 
 
 @pytest.mark.parametrize("case", ["tiny", "single8k", "varlen32k", "zipf64k", "ragged", "topk1", "topk32",
-                                  "ties"])
+                                  "ties", "single8k_b128", "ragged_block128"])
 def test_selection_bit_exact(B, case):
     if case in W.WORKLOADS:
         pb = W.make_problem(case, values=False)
     elif case == "ragged":
         pb = W.make_problem(lengths=[200, 77, 130, 1, 9, 513, 2049], num_index_heads=3, topk=6,
                             policy="diag_uniform", seed=3, values=False)
+    elif case == "ragged_block128":
+        pb = W.make_problem(lengths=[200, 77, 130, 1, 9, 513, 2049], num_index_heads=3, topk=6,
+                            policy="diag_uniform", seed=3, values=False, block=128)
     elif case == "topk1":
         pb = W.make_problem(lengths=[700, 90], num_index_heads=2, topk=1, policy="diag_uniform", seed=4,
                             values=False)

@@ -47,11 +47,25 @@ def _check_tables(B, pb, tile, sms=None):
     return n
 
 
-@pytest.mark.parametrize("name", ["tiny", "single8k", "varlen32k", "zipf64k", "long128k"])
+@pytest.mark.parametrize("name", ["tiny", "single8k", "varlen32k", "zipf64k", "long128k", "single8k_b128",
+                                  "long128k_b128"])
 def test_tables_bit_exact_named(B, name):
     pb = W.make_problem(name, values=False)
-    tile = 1024 if name == "long128k" else 0
+    tile = 1024 if name.startswith("long128k") else 0
     _check_tables(B, pb, tile)
+
+
+@pytest.mark.parametrize("tile", [0, 3])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_tables_bit_exact_ragged_block128(B, tile, seed):
+    # 128-key blocks: documents that end inside a block's lower or upper
+    # half, a single token, and chunks whose last query stops short of the
+    # upper half of their own diagonal block
+    rng = np.random.default_rng(200 + seed)
+    lengths = [65, 127, 1, 129, 200, 64, 700] if seed == 0 else [int(x) for x in rng.integers(1, 1200, size=6)]
+    pb = W.make_problem(lengths=lengths, num_index_heads=2, topk=5, policy="diag_uniform", seed=seed,
+                        values=False, block=128, kv_layout="aligned" if seed else "compact")
+    _check_tables(B, pb, tile, sms=int(rng.integers(1, 200)))
 
 
 @pytest.mark.parametrize("tile", [0, 1, 5, 64])
@@ -134,3 +148,29 @@ def test_inconsistent_documents_set_status(B):
     bw.build_tables(t["sel"])
     torch.cuda.synchronize()
     assert int(bw.status[0].item()) == B.MSA_ERR_INVALID_DOCUMENTS
+
+
+@pytest.mark.slow
+def test_tables_bit_exact_row_windows(B):
+    # more key-block rows than one shared-memory row window of the CSR build
+    # (16384): a 1.1M-token document and a short one, with duplicates planted
+    # past the first window checked separately below
+    pb = W.make_problem(lengths=[1_100_000, 5000], num_index_heads=1, topk=3, policy="diag_uniform", seed=21,
+                        values=False)
+    assert O.DocLayout(pb.cu_seqlens, pb.block, pb.chunk).NB > 16384
+    _check_tables(B, pb, 4096)
+
+
+def test_duplicate_past_the_first_row_window_sets_status(B):
+    import torch
+    pb = W.make_problem(lengths=[1_100_000], num_index_heads=1, topk=3, policy="diag_uniform", seed=22,
+                        values=False)
+    sel = pb.sel.copy()
+    g = sel.shape[1] - 5                       # a late chunk: its diagonal row is in the second window
+    sel[0, g, 1] = sel[0, g, 0]
+    pb.sel = sel
+    prob, t = upload(pb)
+    bw = B.Backward(prob)
+    bw.build_tables(t["sel"])
+    torch.cuda.synchronize()
+    assert int(bw.status[0].item()) == B.MSA_ERR_INVALID_SELECTION
