@@ -16,7 +16,9 @@
 // Q, dO, K, V arrive by TMA with 128-byte swizzle; P and dS are written in the
 // same swizzled layout, so no operand is ever transposed in memory.  A task's
 // dQ (fp32 in TMEM over its 64 keys) is rounded to bf16 and reduced straight
-// into the bf16 dQ output with a TMA bulk reduce-add; dK^T and dV^T stay in
+// into the bf16 dQ output with a TMA bulk reduce-add (or, with the fp32 dQ
+// option, reduce-added in fp32 into a workspace accumulator that the
+// postprocess rounds once); dK^T and dV^T stay in
 // TMEM for a bucket segment and are reduced into fp32 accumulators when the
 // segment ends, which the postprocess casts to bf16.
 #include <cuda.h>
@@ -38,8 +40,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
                                                           float* __restrict__ delta, int64_t T, int Hq,
                                                           float4* __restrict__ zero,
-                                                          int64_t zero_n4, uint4* __restrict__ dq,
-                                                          const int32_t* status) {
+                                                          int64_t zero_n4, uint4* __restrict__ dq_zero,
+                                                          int64_t dq_zero_n16, const int32_t* status) {
   if (status_bad(status)) return;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
@@ -62,9 +64,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
   }
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int64_t i = tid; i < zero_n4; i += nthr) zero[i] = z;
-  // dQ is reduced straight into the bf16 output
+  // the buffer dQ is reduced into: the bf16 output, or the fp32 accumulator
   const uint4 zb = make_uint4(0, 0, 0, 0);
-  for (int64_t i = tid; i < total16; i += nthr) dq[i] = zb;
+  for (int64_t i = tid; i < dq_zero_n16; i += nthr) dq_zero[i] = zb;
 }
 
 // ---------------------------------------------------------------------------
@@ -76,16 +78,21 @@ __device__ __forceinline__ uint4 cast8(const float4* src) {
 }
 
 // The dK, dV accumulators are index-head-major, [Hkv][W][128]; the outputs are
-// [W][Hkv][128].  (dQ needs no postprocess: it is reduced straight into its
-// bf16 output.)
+// [W][Hkv][128].  dQ needs a cast only when it was accumulated in fp32
+// (dq_acc non-null, same layout as the output); otherwise it was reduced
+// straight into its bf16 output.
 __global__ void __launch_bounds__(256) postprocess_kernel(const float4* __restrict__ dk_acc,
                                                            const float4* __restrict__ dv_acc, uint4* __restrict__ dk,
                                                            uint4* __restrict__ dv, int64_t kv_n8, int64_t W, int Hkv,
                                                            const int32_t* cu, const int32_t* kvs, int N,
+                                                           const float4* __restrict__ dq_acc,
+                                                           uint4* __restrict__ dq, int64_t dq_n8,
                                                            const int32_t* status) {
   if (status_bad(status)) return;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
+  if (dq_acc)
+    for (int64_t i = tid; i < dq_n8; i += nthr) dq[i] = cast8(dq_acc + 2 * i);
   const int kv_row_n8 = Hkv * 16;
   for (int64_t i = tid; i < kv_n8; i += nthr) {
     const int64_t row = i / kv_row_n8;
@@ -143,7 +150,9 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
   for (const void* x : ptrs)
     if (!x || !aligned16(x)) return MSA_ERR_INVALID_ARGUMENT;
   if (task_cap < 1 || task_cap > INT32_MAX) return MSA_ERR_INVALID_ARGUMENT;
-  if (ws_bytes < bwd_ws_bytes(p)) return MSA_ERR_INVALID_ARGUMENT;
+  if (stages & ~(uint32_t)(MSA_STAGE_ALL | MSA_BWD_DQ_FP32)) return MSA_ERR_INVALID_ARGUMENT;
+  const bool dq_fp32 = (stages & MSA_BWD_DQ_FP32) != 0;
+  if (ws_bytes < bwd_ws_bytes(p, dq_fp32)) return MSA_ERR_INVALID_ARGUMENT;
   if ((rc = check_device_current())) return rc;
   int32_t sms = 0;
   if ((rc = sm_count_current(&sms))) return rc;
@@ -159,25 +168,31 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
   w += round_up(sizeof(float) * W * Hkv * kHeadDim, 256);
   const int64_t zero_n4 = (reinterpret_cast<float*>(w) - dk_acc) / 4;
   int32_t* unit_ctr = reinterpret_cast<int32_t*>(w);
+  w += 256;
+  float* dq_acc = dq_fp32 ? reinterpret_cast<float*>(w) : nullptr;
 
   // loads: Q/dO boxes of 8 tokens x 16 heads x 64 dims, K/V boxes of 64 keys x 64 dims;
-  // reduce-adds: dQ boxes of 2 tokens x 16 heads x 64 dims (bf16, into the output),
-  // dK/dV of 32 keys x 32 dims (fp32)
+  // reduce-adds: dQ boxes of 2 tokens x 16 heads x 64 dims (bf16, into the output)
+  // or x 32 dims (fp32, into the accumulator), dK/dV of 32 keys x 32 dims (fp32)
   CUtensorMap tmQ, tmdO, tmK, tmV, tmdQ, tmdK, tmdV;
   bool ok = make_tmap_3d(&tmQ, q, false, T, Hq, 64, 16, 8) && make_tmap_3d(&tmdO, dout, false, T, Hq, 64, 16, 8) &&
             make_tmap_3d(&tmK, k, false, W, Hkv, 64, 1, 64) && make_tmap_3d(&tmV, v, false, W, Hkv, 64, 1, 64) &&
-            make_tmap_3d(&tmdQ, dq, false, T, Hq, 64, 16, 2) &&
+            (dq_fp32 ? make_tmap_3d(&tmdQ, dq_acc, true, T, Hq, 32, 16, 2)
+                     : make_tmap_3d(&tmdQ, dq, false, T, Hq, 64, 16, 2)) &&
             make_tmap_3d(&tmdK, dk_acc, true, W * Hkv, 1, 32, 1, 32) &&
             make_tmap_3d(&tmdV, dv_acc, true, W * Hkv, 1, 32, 1, 32);
   if (!ok) return MSA_ERR_CUDA;
 
-  if (stages & ~(uint32_t)MSA_STAGE_ALL) return MSA_ERR_INVALID_ARGUMENT;
+  const int64_t dq_n16 = T * Hq * kHeadDim * 2 / 16;  // 16-byte units of the bf16 dQ
   if (stages & MSA_STAGE_PREPROCESS)
     preprocess_kernel<<<sms * 8, 256, 0, st>>>(
         reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), delta, T, (int)Hq,
-        reinterpret_cast<float4*>(dk_acc), zero_n4, reinterpret_cast<uint4*>(dq), d_status);
+        reinterpret_cast<float4*>(dk_acc), zero_n4,
+        dq_fp32 ? reinterpret_cast<uint4*>(dq_acc) : reinterpret_cast<uint4*>(dq), dq_fp32 ? 2 * dq_n16 : dq_n16,
+        d_status);
   if (stages & MSA_STAGE_MAIN) {
-  if (cudaFuncSetAttribute(bwd_main_ws, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ws::SMEM) != cudaSuccess)
+  auto* kernel = dq_fp32 ? bwd_main_ws<true> : bwd_main_ws<false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ws::SMEM) != cudaSuccess)
     return MSA_ERR_CUDA;
   const int64_t bound = msa_grid_launch_bound(task_cap, sms);
   const int grid = (int)(bound < sms ? (bound < 1 ? 1 : bound) : sms);
@@ -186,13 +201,14 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
   a.kv_doc_starts = p->kv_doc_starts; a.Hq = (int)Hq; a.W = (int)W; a.unit_ctr = unit_ctr; a.scale_log2 = p->softmax_scale * kLog2e;
   a.scale = p->softmax_scale; a.status = d_status;
   if ((rc = cuda_status(cudaMemsetAsync(unit_ctr, 0, sizeof(int32_t), st)))) return rc;
-  bwd_main_ws<<<grid, ws::kThreads, ws::SMEM, st>>>(tmQ, tmdO, tmK, tmV, tmdQ, tmdK, tmdV, a);
+  kernel<<<grid, ws::kThreads, ws::SMEM, st>>>(tmQ, tmdO, tmK, tmV, tmdQ, tmdK, tmdV, a);
   }
   if (stages & MSA_STAGE_POSTPROCESS)
     postprocess_kernel<<<sms * 8, 256, 0, st>>>(
       reinterpret_cast<const float4*>(dk_acc), reinterpret_cast<const float4*>(dv_acc), reinterpret_cast<uint4*>(dk),
       reinterpret_cast<uint4*>(dv), W * Hkv * kHeadDim / 8, W, (int)Hkv, p->cu_seqlens,
-      p->kv_doc_starts, p->num_docs, d_status);
+      p->kv_doc_starts, p->num_docs, reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<uint4*>(dq), dq_n16,
+      d_status);
   return cuda_status(cudaGetLastError());
 }
 

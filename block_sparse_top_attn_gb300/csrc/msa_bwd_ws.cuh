@@ -193,6 +193,10 @@ __device__ __forceinline__ void store_row16(uint8_t* base, int m, int qtr, const
 
 }  // namespace ws
 
+// kDqFp32: dQ tiles are reduce-added in fp32 into the workspace accumulator
+// (tmdQ maps it) instead of in bf16 into the output; two instances, so the
+// default path carries no branch for the option.
+template <bool kDqFp32>
 __global__ void __launch_bounds__(ws::kThreads, 1)
     bwd_main_ws(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -517,38 +521,67 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         const uint32_t pb = j & 1;
         if (!wait_bar_warp(sh, DQ_FULL + pb, (j >> 1) & 1, a.status)) break;
         tc_fence_after();
+        if constexpr (kDqFp32) {
+          // fp32 dQ: four 32-dim pieces, each one 128-byte swizzled fp32 row
+          // per lane of a 2-token x 16-head x 32-dim box
 #pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf, ++chunk) {
-          // 64 dims in two 32-column loads, each packed to bf16 on arrival
-          uint32_t pq[32];
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
+          for (int pc = 0; pc < 4; ++pc, ++chunk) {
             uint32_t v[32];
-            tmem_ld32x(tmem + lane_base + col_dq(pb) + hf * 64 + h2 * 32, v);
+            tmem_ld32x(tmem + lane_base + col_dq(pb) + pc * 32, v);
             tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pq[h2 * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          }
-          if (hf == 1) {
-            tc_fence_before();
+            if (pc == 3) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sh->bar[DQ_EMPTY + pb]);
+            }
+            uint8_t* stg = stg0 + (chunk & 1) * 4096;
+            if (lane == 0) bulk_wait_read_but_one();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sh->bar[DQ_EMPTY + pb]);
-          }
-          // 64 dims of this lane's row as bf16: one 128-byte swizzled row of a
-          // 2-token x 16-head x 64-dim box
-          uint8_t* stg = stg0 + (chunk & 1) * 4096;
-          if (lane == 0) bulk_wait_read_but_one();
-          __syncwarp();
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                make_uint4(pq[4 * c], pq[4 * c + 1], pq[4 * c + 2], pq[4 * c + 3]);
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_reduce_add_3d_hint(&tmdQ, stg, hf * 64, hi * 16, tok0 + 2 * sp, keep);
-            bulk_commit();
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                  make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_3d_hint(&tmdQ, stg, pc * 32, hi * 16, tok0 + 2 * sp, keep);
+              bulk_commit();
+            }
+          }
+        } else {
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf, ++chunk) {
+            // 64 dims in two 32-column loads, each packed to bf16 on arrival
+            uint32_t pq[32];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint32_t v[32];
+              tmem_ld32x(tmem + lane_base + col_dq(pb) + hf * 64 + h2 * 32, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                pq[h2 * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            }
+            if (hf == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sh->bar[DQ_EMPTY + pb]);
+            }
+            // 64 dims of this lane's row as bf16: one 128-byte swizzled row of a
+            // 2-token x 16-head x 64-dim box
+            uint8_t* stg = stg0 + (chunk & 1) * 4096;
+            if (lane == 0) bulk_wait_read_but_one();
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                  make_uint4(pq[4 * c], pq[4 * c + 1], pq[4 * c + 2], pq[4 * c + 3]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_3d_hint(&tmdQ, stg, hf * 64, hi * 16, tok0 + 2 * sp, keep);
+              bulk_commit();
+            }
           }
         }
         if (flags & 2) {

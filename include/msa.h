@@ -113,6 +113,11 @@ enum {
  * Returns 0 if the problem is invalid. */
 size_t msa_workspace_bytes(const msa_problem* p, int64_t edge_cap, int64_t task_cap,
                            int32_t task_tile_chunks);
+/* msa_workspace_bytes for a backward run with options (MSA_BWD_DQ_FP32 adds
+ * an fp32 dQ accumulator of T * Hq * 128 * 4 bytes).  Returns 0 for an
+ * invalid problem or an unknown option bit. */
+size_t msa_workspace_bytes_opts(const msa_problem* p, int64_t edge_cap, int64_t task_cap,
+                                int32_t task_tile_chunks, uint32_t options);
 
 /* Key-block -> query CSR ("msa_bindings" page, build_k2q_csr;
  * "msa_schedule" page, row_ptr and q_indices).
@@ -212,6 +217,16 @@ int msa_bwd(const msa_problem* p, const uint16_t* q, const uint16_t* k, const ui
  * stages = MSA_STAGE_ALL.  The stages communicate through ws, so a later
  * stage must see the same ws, tables and inputs as the earlier ones. */
 enum { MSA_STAGE_PREPROCESS = 1, MSA_STAGE_MAIN = 2, MSA_STAGE_POSTPROCESS = 4, MSA_STAGE_ALL = 7 };
+/* Option bit of the same mask: accumulate dQ in fp32.  By default each
+ * task's fp32 dQ (over its 64 keys) is rounded to bf16 and reduce-added into
+ * the bf16 dQ output, as the pages' bf16 dQ pool is ("msa_schedule" page,
+ * the bf16x2 dQ pool; "msa_backward_sm100" page, dQ atomics), so a row of dQ
+ * takes one bf16 rounding per task that feeds it.  With MSA_BWD_DQ_FP32 the
+ * tasks reduce-add fp32 tiles into an fp32 buffer in ws (twice the reduce
+ * traffic), which the postprocess rounds once to bf16.  ws must then hold
+ * msa_workspace_bytes_opts(..., MSA_BWD_DQ_FP32) bytes, and every stage of
+ * one backward must be called with the same option. */
+enum { MSA_BWD_DQ_FP32 = 8 };
 int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                    const uint16_t* o, const uint16_t* dout, const float* lse, const int32_t* task_meta,
                    const int32_t* task_q_rows, const int32_t* task_q_pos, const int32_t* walk,

@@ -83,6 +83,29 @@ def test_invalid_arguments_rejected_on_host(B):
     assert lib.msa_workspace_bytes(ctypes.byref(p), 64, 8, 0) == 0
 
 
+def test_block_size_and_workspace_options(B):
+    """Block sizes 64 and 128 are accepted, others rejected; the fp32 dQ option
+    adds one fp32 [T, Hq, 128] accumulator to the workspace; unknown option
+    bits are rejected (fake, never dereferenced addresses)."""
+    lib = B.lib
+    p = B.msa_problem()
+    p.num_docs, p.total_tokens, p.kv_rows = 1, 4096, 4096
+    p.cu_seqlens, p.kv_doc_starts = 4096, 8192
+    p.num_q_heads, p.num_index_heads, p.num_kv_heads = 64, 4, 4
+    p.head_dim, p.block_size, p.query_chunk, p.topk = 128, 64, 8, 4
+    p.num_blocks, p.num_chunks, p.softmax_scale = 64, 512, 0.1
+    base = lib.msa_workspace_bytes(ctypes.byref(p), 64, 8, 0)
+    assert base > 0 and lib.msa_workspace_bytes_opts(ctypes.byref(p), 64, 8, 0, 0) == base
+    assert lib.msa_workspace_bytes_opts(ctypes.byref(p), 64, 8, 0, B.MSA_BWD_DQ_FP32) == base + 4096 * 64 * 128 * 4
+    assert lib.msa_workspace_bytes_opts(ctypes.byref(p), 64, 8, 0, 16) == 0
+    p.block_size, p.num_blocks = 128, 32
+    assert lib.msa_workspace_bytes(ctypes.byref(p), 64, 8, 0) > 0
+    p.block_size, p.num_blocks = 96, 43
+    assert lib.msa_workspace_bytes(ctypes.byref(p), 64, 8, 0) == 0
+    p.block_size, p.num_blocks = 128, 64     # block count of 64-key blocks with 128-key blocks
+    assert lib.msa_workspace_bytes(ctypes.byref(p), 64, 8, 0) == 0
+
+
 def test_forward_arguments_rejected_on_host(B):
     """msa_fwd rejects a null problem, null or misaligned buffers and a short
     workspace before it touches the device (fake, never dereferenced addresses)."""

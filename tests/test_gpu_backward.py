@@ -23,22 +23,22 @@ def B():
     return binding
 
 
-def _run_gpu(B, pb, o_bits, lse32, tile=0):
+def _run_gpu(B, pb, o_bits, lse32, tile=0, dq_fp32=False):
     import torch
     prob, t = upload(pb)
     o = to_bf16_tensor(o_bits, "cuda")
     lse = torch.from_numpy(np.ascontiguousarray(lse32)).cuda()
-    bw = B.Backward(prob, task_tile_chunks=tile)
+    bw = B.Backward(prob, task_tile_chunks=tile, dq_fp32=dq_fp32)
     dq, dk, dv = bw.run(t["sel"], t["q"], t["k"], t["v"], o, t["do"], lse)
     torch.cuda.synchronize()
     bw.check_status()
     return from_bf16_tensor(dq), from_bf16_tensor(dk), from_bf16_tensor(dv)
 
 
-def _parity(B, pb, tile=0):
+def _parity(B, pb, tile=0, dq_fp32=False):
     o_bits, lse32 = oracle_forward_stored(pb)
     ref = oracle_backward(pb, o_bits, lse32)
-    got = _run_gpu(B, pb, o_bits, lse32, tile)
+    got = _run_gpu(B, pb, o_bits, lse32, tile, dq_fp32)
     out = {}
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
         out[name] = assert_grad_close(name, g, r)
@@ -54,10 +54,38 @@ def test_backward_single8k(B, tile):
     _parity(B, W.make_problem("single8k"), tile)
 
 
-@pytest.mark.parametrize("case", ["ragged_aligned", "single_tokens", "topk1", "empty_chunks", "tail_T"])
+def test_backward_single8k_block128(B):
+    _parity(B, W.make_problem("single8k_b128"), 16)
+
+
+@pytest.mark.parametrize("case", ["tiny", "single8k", "ragged_aligned"])
+def test_backward_dq_fp32(B, case):
+    """The fp32 dQ accumulator option: same tolerances, and dQ's error should
+    not exceed the bf16 reduce-add path's."""
+    if case == "ragged_aligned":
+        pb = W.make_problem(lengths=[200, 77, 130, 1, 9, 513], num_index_heads=2, topk=4, policy="diag_uniform",
+                            kv_layout="aligned", seed=1)
+    else:
+        pb = W.make_problem(case)
+    _parity(B, pb, 16, dq_fp32=True)
+
+
+@pytest.mark.slow
+def test_backward_dq_fp32_zipf64k(B):
+    _parity(B, W.make_problem("zipf64k"), tile=512, dq_fp32=True)
+
+
+@pytest.mark.parametrize("case", ["ragged_aligned", "single_tokens", "topk1", "empty_chunks", "tail_T",
+                                  "block128_ragged_aligned", "block128_tail"])
 def test_backward_edge_cases(B, case):
     rng = np.random.default_rng(7)
-    if case == "ragged_aligned":
+    if case == "block128_ragged_aligned":
+        pb = W.make_problem(lengths=[65, 127, 1, 129, 200, 513], num_index_heads=2, topk=3, policy="diag_uniform",
+                            kv_layout="aligned", seed=11, block=128)
+    elif case == "block128_tail":
+        pb = W.make_problem(lengths=[555], num_index_heads=1, topk=4, policy="diag_recent3_uniform", seed=12,
+                            block=128)
+    elif case == "ragged_aligned":
         pb = W.make_problem(lengths=[200, 77, 130, 1, 9, 513], num_index_heads=2, topk=4, policy="diag_uniform",
                             kv_layout="aligned", seed=1)
     elif case == "single_tokens":
@@ -85,7 +113,8 @@ def test_backward_full_oracle_large(B, name):
 
 
 @pytest.mark.slow
-def test_backward_long128k_sampled(B):
+@pytest.mark.parametrize("name,dq_fp32", [("long128k", False), ("long128k", True), ("long128k_b128", False)])
+def test_backward_long128k_sampled(B, name, dq_fp32):
     """Full-size long-context workload in the launch configuration the bench
     times.  The backward takes O and LSE as inputs: msa_fwd supplies them for
     every row, then every (index head, chunk) that feeds a sampled output gets
@@ -93,7 +122,7 @@ def test_backward_long128k_sampled(B):
     differentiate at the same point and nothing flows from the device into the
     oracle."""
     import torch
-    pb = W.make_problem("long128k")
+    pb = W.make_problem(name)
     prob, t = upload(pb)
     o, lse, st = B.forward(prob, t["sel"], t["q"], t["k"], t["v"])
     torch.cuda.synchronize()
@@ -102,7 +131,8 @@ def test_backward_long128k_sampled(B):
     G = pb.num_q_heads // pb.sel.shape[0]
     rng = np.random.default_rng(0)
     qpicks = [(0, int(rng.integers(0, 8)), int(c)) for c in rng.integers(0, lay.NC, size=12)] + [(0, 3, 0), (0, 7, lay.NC - 1)]
-    kpicks = [(0, 0, 0), (0, 5, int(lay.nb[0]) - 1), (0, 2, 1000), (0, int(rng.integers(0, 8)), int(rng.integers(0, 2048)))]
+    kpicks = [(0, 0, 0), (0, 5, int(lay.nb[0]) - 1), (0, 2, int(lay.nb[0]) // 2 - 24),
+              (0, int(rng.integers(0, 8)), int(rng.integers(0, int(lay.nb[0]))))]
     units = {(hi, c) for _, hi, c in qpicks}
     for _, hi, b in kpicks:                 # one document: global chunk = local chunk
         units |= {(hi, int(c)) for c in np.nonzero((pb.sel[hi] == b).any(axis=1))[0]}
@@ -111,7 +141,7 @@ def test_backward_long128k_sampled(B):
         rows = torch.from_numpy(int(lay.cu[0]) + qp).cuda()
         o[rows, hi * G:(hi + 1) * G] = to_bf16_tensor(O.f64_to_bf16(oc.transpose(1, 0, 2)), "cuda")
         lse[rows, hi * G:(hi + 1) * G] = torch.from_numpy(np.ascontiguousarray(lc.T).astype(np.float32)).cuda()
-    bw = B.Backward(prob, task_tile_chunks=1024)
+    bw = B.Backward(prob, task_tile_chunks=1024, dq_fp32=dq_fp32)
     dq, dk, dv = bw.run(t["sel"], t["q"], t["k"], t["v"], o, t["do"], lse)
     torch.cuda.synchronize()
     bw.check_status()
