@@ -299,7 +299,7 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     pb = W.make_problem(args.workload, values=False, seed=rank)
     prob = B.make_problem(pb.cu_seqlens, pb.kv_doc_starts, pb.kv_rows, pb.num_q_heads, pb.topk, pb.softmax_scale,
-                          device=dev)
+                          device=dev, block_size=pb.block)
     sel = torch.from_numpy(pb.sel).to(dev)
     q, k, v, do = W.device_values(pb, dev, seed=rank)
     o, lse, st = B.forward(prob, sel, q, k, v)
@@ -487,6 +487,25 @@ def run_gpu(args):
     h2d_ms = sum(a_.elapsed_time(b_) for a_, b_ in h2d_ev)
     d2h_ms = sum(a_.elapsed_time(b_) for a_, b_ in d2h_ev)
 
+    # The fp32 dQ accumulator option on the same tables: preprocess, main and
+    # postprocess timed with events, after one untimed backward.
+    del bws
+    bw32 = B.Backward(prob, task_tile_chunks=args.tile, dq_fp32=True)
+    bw32.build_tables(sel)
+    bw32.backward(q, k, v, o, do, lse)
+    reps32 = 2
+    ev32 = [[ev() for _ in range(4)] for _ in range(reps32)]
+    for e in ev32:
+        e[0].record(stream)
+        for i_, stage_ in enumerate((B.MSA_STAGE_PREPROCESS, B.MSA_STAGE_MAIN, B.MSA_STAGE_POSTPROCESS)):
+            bw32.backward_stage(stage_, q, k, v, o, do, lse)
+            e[i_ + 1].record(stream)
+    torch.cuda.synchronize()
+    bw32.check_status()
+    dq32_ms = {name: sum(e[i].elapsed_time(e[i + 1]) for e in ev32) / reps32
+               for i, name in enumerate(("preprocess", "main", "postprocess"))}
+    del bw32
+
     burst, sustained, hbm, src = _peaks()
     achieved = flop / (main_ms * 1e-3) / 1e12
     traffic, traffic_note = traffic_record(args.workload, args.tile)
@@ -535,6 +554,10 @@ def run_gpu(args):
                                  "bound": "alu", "fp32_fma_peak_tflops": FP32_FMA_PEAK_TFLOPS,
                                  "frac": score_flop / (score_ms * 1e-3) / 1e12 / FP32_FMA_PEAK_TFLOPS,
                                  "timed": "3 msa_select_topk calls on seeded index projections after one warm-up"},
+                      "dq_fp32": {"stages_ms": dq32_ms, "step_ms": sum(dq32_ms.values()),
+                                  "main_tflops": flop / (dq32_ms["main"] * 1e-3) / 1e12,
+                                  "timed": "2 x (preprocess, main, postprocess) with the fp32 dQ accumulator "
+                                           "option, after one untimed backward"},
                       "aux_kernels": aux},
         "clocks": clocks,
     }
@@ -552,6 +575,46 @@ def run_gpu(args):
     return 0
 
 
+def run_tables(args):
+    """The CSR and task builds alone on the workload's selection (no dense
+    tensors on the device): per-stage CUDA-event times and GB/s of the
+    algorithmic bytes.  For profiling the table kernels on a small footprint."""
+    import torch
+    from block_sparse_top_attn_gb300 import binding as B
+    from block_sparse_top_attn_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pb = W.make_problem(args.workload, values=False)
+    prob = B.make_problem(pb.cu_seqlens, pb.kv_doc_starts, pb.kv_rows, pb.num_q_heads, pb.topk, pb.softmax_scale,
+                          device=dev, block_size=pb.block)
+    sel = torch.from_numpy(pb.sel).to(dev)
+    bw = B.Backward(prob, task_tile_chunks=args.tile)
+    stream = torch.cuda.current_stream()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        bw.build_tables(sel)
+    torch.cuda.synchronize()
+    for e in evs:
+        e[0].record(stream)
+        B.msa_build_k2q(bw.p, sel, bw.row_ptr, bw.q_indices, bw.edge_cap, bw.status, bw.ws)
+        e[1].record(stream)
+        B.msa_build_tasks(bw.p, bw.row_ptr, bw.q_indices, bw.edge_cap, bw.tile, bw.task_meta, bw.task_q_rows,
+                          bw.task_q_pos, bw.walk, bw.task_cap, bw.num_sms, bw.status, bw.ws)
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    bw.check_status()
+    n_tasks = bw.num_tasks()
+    ms = {name: sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps for i, name in enumerate(("k2q", "tasks"))}
+    ab = aux_bytes(pb, n_tasks)
+    _, _, hbm, _ = _peaks()
+    out = {"metric": "CSR and task build time", "unit": "ms", "workload": args.workload, "tasks": n_tasks,
+           "steps": args.steps, "warmup": args.warmup,
+           "stages": {k: {"ms": ms[k], "algorithmic_bytes": ab[k], "gbs": ab[k] / (ms[k] * 1e-3) / 1e9,
+                          "frac_of_hbm": ab[k] / (ms[k] * 1e-3) / 1e9 / hbm} for k in ms}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -563,9 +626,13 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tables-only", action="store_true",
+                    help="time only the CSR and task builds (a small footprint, for profiling them)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.tables_only:
+        return run_tables(args)
     return run_gpu(args)
 
 
