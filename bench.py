@@ -576,9 +576,11 @@ def run_gpu(args):
 
 
 def run_tables(args):
-    """The CSR and task builds alone on the workload's selection (no dense
-    tensors on the device): per-stage CUDA-event times and GB/s of the
-    algorithmic bytes.  For profiling the table kernels on a small footprint."""
+    """The index-side kernels alone (no attention tensors on the device): the
+    CSR and task builds on the workload's selection (per-stage CUDA-event
+    times and GB/s of the algorithmic bytes), the scorer + top-k on seeded
+    index projections and the forward planner.  For profiling those kernels
+    on a small footprint."""
     import torch
     from block_sparse_top_attn_gb300 import binding as B
     from block_sparse_top_attn_gb300 import workloads as W
@@ -605,12 +607,34 @@ def run_tables(args):
     bw.check_status()
     n_tasks = bw.num_tasks()
     ms = {name: sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps for i, name in enumerate(("k2q", "tasks"))}
+    # the scorer + top-k and the forward planner on the same problem
+    qi_idx, ki_idx = W.device_index_values(pb, dev, seed=0)
+    sel2 = torch.empty_like(sel)
+    meta = torch.empty((pb.num_index_heads * pb.sel.shape[1], B.MSA_TASK_META_COLS), dtype=torch.int32, device=dev)
+    wc = torch.zeros(4, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup):
+        B.msa_select_topk(prob, qi_idx, ki_idx, sel2, bw.status, bw.ws)
+        B.msa_plan_forward(prob, sel, meta, wc, bw.status, bw.ws)
+    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for e in ev2:
+        e[0].record(stream)
+        B.msa_select_topk(prob, qi_idx, ki_idx, sel2, bw.status, bw.ws)
+        e[1].record(stream)
+        B.msa_plan_forward(prob, sel, meta, wc, bw.status, bw.ws)
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    bw.check_status()
+    ms2 = {name: sum(e[i].elapsed_time(e[i + 1]) for e in ev2) / args.steps for i, name in enumerate(("scorer", "plan"))}
     ab = aux_bytes(pb, n_tasks)
     _, _, hbm, _ = _peaks()
+    sf = scorer_flops(pb)
     out = {"metric": "CSR and task build time", "unit": "ms", "workload": args.workload, "tasks": n_tasks,
            "steps": args.steps, "warmup": args.warmup,
            "stages": {k: {"ms": ms[k], "algorithmic_bytes": ab[k], "gbs": ab[k] / (ms[k] * 1e-3) / 1e9,
-                          "frac_of_hbm": ab[k] / (ms[k] * 1e-3) / 1e9 / hbm} for k in ms}}
+                          "frac_of_hbm": ab[k] / (ms[k] * 1e-3) / 1e9 / hbm} for k in ms},
+           "scorer": {"ms": ms2["scorer"], "score_gflop": sf / 1e9,
+                      "frac_of_fp32_fma_peak": sf / (ms2["scorer"] * 1e-3) / 1e12 / FP32_FMA_PEAK_TFLOPS},
+           "plan": {"ms": ms2["plan"]}}
     print(json.dumps(out), flush=True)
     return 0
 
@@ -627,7 +651,7 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tables-only", action="store_true",
-                    help="time only the CSR and task builds (a small footprint, for profiling them)")
+                    help="time only the index-side kernels: CSR, tasks, scorer, planner (a small footprint)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
