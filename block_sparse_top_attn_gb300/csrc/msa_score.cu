@@ -17,8 +17,8 @@
 //
 // Kernels: pool_kernel (one warp per chunk or block and index head; HBM-bound)
 // and topk_kernel (a CTA scores 32 chunks against 64-block tiles with a 4 x 2
-// register tile per thread, then each warp merges its rows' candidates into
-// per-row top-(K-1) lists held one entry per lane).
+// register tile per thread, four dims per step, then each warp merges its
+// rows' candidates into per-row top-(K-1) lists held one entry per lane).
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -69,7 +69,8 @@ __global__ void __launch_bounds__(256) pool_kernel(PoolArgs a) {
     const int n = min(a.size, len - first);
     const uint16_t* src = a.x + ((int64_t)(a.cu[d] + first) * a.Hi + hi) * kDim + lane * 4;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int t = 0; t < n; ++t) {
+#pragma unroll 8
+    for (int t = 0; t < n; ++t) {  // loads run ahead of the in-order sums
       const uint2 v = *reinterpret_cast<const uint2*>(src + (int64_t)t * a.Hi * kDim);
       acc[0] = __fadd_rn(acc[0], __uint_as_float(v.x << 16));
       acc[1] = __fadd_rn(acc[1], __uint_as_float(v.x & 0xFFFF0000u));
@@ -163,17 +164,25 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     __syncthreads();
     // 4 rows (4 warp .. 4 warp + 3) x 2 blocks (b0 + 2 lane, + 1), summed over
     // the dims in ascending order
+    // (four dims per step: a row's four query values in one 16-byte load, so
+    // eight shared-memory loads feed 32 FMAs)
     float s[4][2];
 #pragma unroll
     for (int i = 0; i < 4; ++i) s[i][0] = s[i][1] = 0.f;
-#pragma unroll 8
-    for (int d = 0; d < kDim; ++d) {
-      const float2 kv = *reinterpret_cast<const float2*>(&sk[d][2 * lane]);
+#pragma unroll 2
+    for (int d = 0; d < kDim; d += 4) {
+      float2 kv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) kv[e] = *reinterpret_cast<const float2*>(&sk[d + e][2 * lane]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float qv = sq[4 * warp + i][d];
-        s[i][0] = __fmaf_rn(qv, kv.x, s[i][0]);
-        s[i][1] = __fmaf_rn(qv, kv.y, s[i][1]);
+        const float4 q4 = *reinterpret_cast<const float4*>(&sq[4 * warp + i][d]);
+        const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          s[i][0] = __fmaf_rn(qv[e], kv[e].x, s[i][0]);
+          s[i][1] = __fmaf_rn(qv[e], kv[e].y, s[i][1]);
+        }
       }
     }
     // merge each row's candidates of this tile into its list
