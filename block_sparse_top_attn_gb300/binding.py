@@ -30,6 +30,7 @@ MSA_NOALLOC_SCRATCH_BYTES = 16 << 20
 MSA_TASK_META_COLS = 6
 MSA_STAGE_PREPROCESS, MSA_STAGE_MAIN, MSA_STAGE_POSTPROCESS, MSA_STAGE_ALL = 1, 2, 4, 7
 MSA_BWD_DQ_FP32 = 8
+MSA_BWD_SELFTEST_HOLD_REDUCE = 16
 MSA_WALK_LEN = 8
 
 HEAD_DIM, BLOCK, CHUNK, GROUP = 128, 64, 8, 16

@@ -150,8 +150,11 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
   for (const void* x : ptrs)
     if (!x || !aligned16(x)) return MSA_ERR_INVALID_ARGUMENT;
   if (task_cap < 1 || task_cap > INT32_MAX) return MSA_ERR_INVALID_ARGUMENT;
-  if (stages & ~(uint32_t)(MSA_STAGE_ALL | MSA_BWD_DQ_FP32)) return MSA_ERR_INVALID_ARGUMENT;
+  if (stages & ~(uint32_t)(MSA_STAGE_ALL | MSA_BWD_DQ_FP32 | MSA_BWD_SELFTEST_HOLD_REDUCE))
+    return MSA_ERR_INVALID_ARGUMENT;
   const bool dq_fp32 = (stages & MSA_BWD_DQ_FP32) != 0;
+  const bool hold = (stages & MSA_BWD_SELFTEST_HOLD_REDUCE) != 0;
+  if (hold && dq_fp32) return MSA_ERR_INVALID_ARGUMENT;
   if (ws_bytes < bwd_ws_bytes(p, dq_fp32)) return MSA_ERR_INVALID_ARGUMENT;
   if ((rc = check_device_current())) return rc;
   int32_t sms = 0;
@@ -191,7 +194,7 @@ extern "C" int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uin
         dq_fp32 ? reinterpret_cast<uint4*>(dq_acc) : reinterpret_cast<uint4*>(dq), dq_fp32 ? 2 * dq_n16 : dq_n16,
         d_status);
   if (stages & MSA_STAGE_MAIN) {
-  auto* kernel = dq_fp32 ? bwd_main_ws<true> : bwd_main_ws<false>;
+  auto* kernel = hold ? bwd_main_ws<false, true> : dq_fp32 ? bwd_main_ws<true> : bwd_main_ws<false>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ws::SMEM) != cudaSuccess)
     return MSA_ERR_CUDA;
   const int64_t bound = msa_grid_launch_bound(task_cap, sms);

@@ -195,8 +195,10 @@ __device__ __forceinline__ void store_row16(uint8_t* base, int m, int qtr, const
 
 // kDqFp32: dQ tiles are reduce-added in fp32 into the workspace accumulator
 // (tmdQ maps it) instead of in bf16 into the output; two instances, so the
-// default path carries no branch for the option.
-template <bool kDqFp32>
+// default path carries no branch for the option.  kHoldReduce (a self-test of
+// the bounded waits, never a result): the reduce warps stay idle, so the
+// hand-offs that wait for them run out their limit and every role aborts.
+template <bool kDqFp32, bool kHoldReduce = false>
 __global__ void __launch_bounds__(ws::kThreads, 1)
     bwd_main_ws(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -511,6 +513,7 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
       // task of the chunk; a dK/dV tile one per bucket segment
       const uint64_t keep = l2_evict_last(), stream = l2_evict_first();
       for (uint32_t j = 0;; ++j) {
+        if (kHoldReduce) break;
         const uint32_t slot = j % kInfo;
         if (!wait_bar_warp(sh, INFO_FULL + slot, (j / kInfo) & 1, a.status)) break;
         const TaskInfo& e = sh->info[slot];

@@ -227,6 +227,13 @@ enum { MSA_STAGE_PREPROCESS = 1, MSA_STAGE_MAIN = 2, MSA_STAGE_POSTPROCESS = 4, 
  * msa_workspace_bytes_opts(..., MSA_BWD_DQ_FP32) bytes, and every stage of
  * one backward must be called with the same option. */
 enum { MSA_BWD_DQ_FP32 = 8 };
+/* Self-test bit of the same mask (no counterpart in the pages; outputs are
+ * not to be used): the main stage runs with its reduce warps idle, so the
+ * hand-offs that wait for them (the task-info ring, the dQ buffers) run out
+ * their 2 s bound, every role of the kernel aborts, in-flight copies are
+ * waited for, and *d_status reads MSA_ERR_TIMEOUT.  The context stays usable.
+ * Not combinable with MSA_BWD_DQ_FP32 (MSA_ERR_INVALID_ARGUMENT). */
+enum { MSA_BWD_SELFTEST_HOLD_REDUCE = 16 };
 int msa_bwd_staged(const msa_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                    const uint16_t* o, const uint16_t* dout, const float* lse, const int32_t* task_meta,
                    const int32_t* task_q_rows, const int32_t* task_q_pos, const int32_t* walk,
