@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kCountThreads) k2q_count_kernel(K2QArgs a) {
 #pragma unroll
         for (int i = 0; i < kCountSlots; ++i) {
           x[i] = -1;
-          const int b = jv ? S.sel[c * kSelStride + w + 8 * i] : -1;
+          const int b = jv ? S.sel[c * kSelStride + w + (kCountThreads / 32) * i] : -1;
           if (b == -1) continue;
           if (b < 0 || b >= nbd || (int64_t)b * a.B > v0) {
             set_status(a.status, MSA_ERR_INVALID_SELECTION);
@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(kScatterThreads) k2q_scatter_kernel(K2QArgs a)
         int x[kScatterSlots];  // row - w0 of each of this thread's entries, or -1
 #pragma unroll
         for (int i = 0; i < kScatterSlots; ++i) {
-          const int b = jv ? S.sel[c * kSelStride + w + 4 * i] : -1;
+          const int b = jv ? S.sel[c * kSelStride + w + (kScatterThreads / 32) * i] : -1;
           const int xr = rb + b;
           x[i] = (b >= 0 && xr >= 0 && xr < w1 - w0) ? xr : -1;
           if (x[i] >= 0) atomicOr(&mask[x[i]], bit);
