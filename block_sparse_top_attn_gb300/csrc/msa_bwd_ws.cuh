@@ -23,14 +23,13 @@
 //               while the reduce-add of the other is still reading) -> TMA
 //               bulk reduce-add.
 //
-// MMAs that accumulate into the same TMEM tile issue back to back only at
-// that tile's accumulate latency (about twice the issue interval of
-// independent MMAs at N = 64), so each issuer interleaves its GEMMs K step by
-// K step: S with dP, and dV^T with dK^T and dQ.
+// Each issuer interleaves two independent accumulators K step by K step: S
+// with dP, and dV^T with dK^T; issuer B then issues dQ.
 //
-// A task's Q/dO stage is held from its TMA load until its last MMA.  dQ is
-// double-buffered in TMEM, so the dQ MMAs of task j+1 never wait for the
-// drain of task j.
+// A task's Q/dO stage is held from its TMA load until its dV^T and dK^T MMAs
+// have run (dQ reads only dS and K), so the next task's load into that stage
+// starts before the dQ MMAs.  dQ is double-buffered in TMEM, so the dQ MMAs
+// of task j+1 never wait for the drain of task j.
 //
 // TMEM (512 columns): S at 0, dP at 64, dQ[2] at 128/256 (128 cols each),
 // dK^T at 384, dV^T at 448 (64 cols each; lane = head-dim index).
@@ -380,9 +379,11 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           }
           __syncwarp();
         } else {
-          // dV^T += dO^T P, dK^T += Q^T dS and dQ = dS K, interleaved.  P/dS
-          // are stored after S/dP completed, so every MMA of the task that
-          // reads this Q/dO stage has completed by the commits below.
+          // dV^T += dO^T P and dK^T += Q^T dS, interleaved, then dQ = dS K.
+          // P/dS are stored after S/dP completed, so once dV and dK have run
+          // no MMA of the task reads this Q/dO stage any more: it is released
+          // before dQ (which reads dS and K only), and the next load into it
+          // starts a dQ group earlier.
           if (!wait_bar_warp(sh, PDS_FULL, j & 1, a.status)) break;
           if (first && !wait_bar_warp(sh, DKV_EMPTY, (seg & 1) ^ 1, a.status)) break;
           if (!wait_bar_warp(sh, DQ_EMPTY + st, ph ^ 1, a.status)) break;
@@ -400,11 +401,12 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
             for (int kk = 0; kk < 8; ++kk) {
               umma_bf16(tmem + COL_DV, dom + kk * 128, pm + kk * 128, ID_T, kk > 0 ? 1u : acc0);
               umma_bf16(tmem + COL_DK, qm + kk * 128, dsm + kk * 128, ID_T, kk > 0 ? 1u : acc0);
-              if (kk & 1) umma_bf16(dq, dsk + (kk >> 1) * 2, km + (kk >> 1) * 128, ID_Q, kk > 1);
             }
-            umma_commit(&sh->bar[PDS_EMPTY]);
             umma_commit(&sh->bar[Q_EMPTY + st]);
             umma_commit(&sh->bar[DO_EMPTY + st]);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) umma_bf16(dq, dsk + k4 * 2, km + k4 * 128, ID_Q, k4 > 0);
+            umma_commit(&sh->bar[PDS_EMPTY]);
             umma_commit(&sh->bar[DQ_FULL + st]);
             if (last) {
               umma_commit(&sh->bar[K_EMPTY]);

@@ -86,7 +86,8 @@ def _simulate(n_tasks, seed, swap_release=False):
     smPdS = [None]
     tmDQ = [None, None]
     tmDKV = [None]                    # segment whose dK/dV accumulate in TMEM
-    doneA, doneB = set(), set()       # completed GEMM groups (S/dP; dV/dK/dQ)
+    doneA, doneB = set(), set()       # completed GEMM groups (S/dP; dV/dK and dQ)
+    releasedB = set()                 # tasks whose dV/dK completed (Q/dO stage released)
     sdp_read, pds_written = {}, {}    # task -> softmax warps done reading S/dP / writing P/dS
     dq_read, dkv_read = {}, {}        # task / segment -> reduce warps done
     qA, qB, tma = [], [], []
@@ -163,7 +164,8 @@ def _simulate(n_tasks, seed, swap_release=False):
                     yield
             while not B[f"dq_empty{st}"].ready_parity(((j >> 1) & 1) ^ 1, (j >> 1) - 1):
                 yield
-            qB.append(("dVdKdQ", j))
+            qB.append(("dVdK", j))
+            qB.append(("dQ", j))
         yield from get_info("B", n_tasks)
 
     def softmax(w):
@@ -223,20 +225,27 @@ def _simulate(n_tasks, seed, swap_release=False):
 
     def run_b():
         if qB and rng.random() < 0.3:
-            _, j = qB.pop(0)
+            kind, j = qB.pop(0)
             seg, first, last = tasks[j]
             assert smPdS[0] == j and pds_written.get(j, 0) == N_SOFT, "dV/dK/dQ before P/dS were stored"
-            assert smQ[j & 1] == j and smDO[j & 1] == j, "dV/dK/dQ after the Q/dO stage was reloaded"
+            if kind == "dVdK":
+                # dV^T and dK^T read the Q/dO stage, P and dS; the stage is
+                # released when they complete
+                assert smQ[j & 1] == j and smDO[j & 1] == j, "dV/dK after the Q/dO stage was reloaded"
+                if first:
+                    assert seg == 0 or dkv_read.get(seg - 1, 0) == N_RED, "dK/dV overwritten before drained"
+                    tmDKV[0] = seg
+                releasedB.add(j)
+                for n in ([f"do_empty{j & 1}", f"q_empty{j & 1}"] if swap_release else
+                          [f"q_empty{j & 1}", f"do_empty{j & 1}"]):
+                    B[n].arrive()
+                return
+            # dQ reads dS and K
             assert smKV[0] == seg, "dQ after K was reloaded"
             assert j < 2 or dq_read.get(j - 2, 0) == N_RED, "dQ over a buffer not yet drained"
-            if first:
-                assert seg == 0 or dkv_read.get(seg - 1, 0) == N_RED, "dK/dV overwritten before drained"
-                tmDKV[0] = seg
             tmDQ[j & 1] = j
             doneB.add(j)
-            for n in (["pds_empty", f"do_empty{j & 1}", f"q_empty{j & 1}"] if swap_release else
-                      ["pds_empty", f"q_empty{j & 1}", f"do_empty{j & 1}"]):
-                B[n].arrive()
+            B["pds_empty"].arrive()
             B[f"dq_full{j & 1}"].arrive()
             if last:
                 B["k_empty"].arrive()
@@ -251,11 +260,11 @@ def _simulate(n_tasks, seed, swap_release=False):
                 smKV[0] = x
                 B["kv"].arrive()
             elif kind == "q":
-                assert x < 2 or ((x - 2) in doneA and (x - 2) in doneB), "Q stage reloaded too early"
+                assert x < 2 or ((x - 2) in doneA and (x - 2) in releasedB), "Q stage reloaded too early"
                 smQ[x & 1] = x
                 B[f"q_full{x & 1}"].arrive()
             else:
-                assert x < 2 or ((x - 2) in doneA and (x - 2) in doneB), "dO stage reloaded too early"
+                assert x < 2 or ((x - 2) in doneA and (x - 2) in releasedB), "dO stage reloaded too early"
                 smDO[x & 1] = x
                 B[f"do_full{x & 1}"].arrive()
 
