@@ -8,7 +8,8 @@
 //               task tables from global memory on its critical path.
 //   warp 1      TMA producer: K/V once per bucket segment, Q/dO per task into
 //               a 2-stage ring.
-//   warp 2      MMA issuer A: S = Q K^T and dP = dO V^T.
+//   warp 2      MMA issuer A: S = Q K^T as soon as Q has landed, then
+//               dP = dO V^T once dO has.
 //   warp 3      MMA issuer B: dV^T += dO^T P, dK^T += Q^T dS and
 //               dQ = dS K.  Two issuing threads keep the tensor core fed while
 //               each waits on its own dependencies; their TMEM targets are
@@ -23,8 +24,9 @@
 //               while the reduce-add of the other is still reading) -> TMA
 //               bulk reduce-add.
 //
-// Each issuer interleaves two independent accumulators K step by K step: S
-// with dP, and dV^T with dK^T; issuer B then issues dQ.
+// Issuer A issues S, then dP (each its own accumulator chain, so S can start
+// before the dO tile lands); issuer B interleaves dV^T with dK^T K step by K
+// step, then issues dQ.
 //
 // A task's Q/dO stage is held from its TMA load until its dV^T and dK^T MMAs
 // have run (dQ reads only dS and K), so the next task's load into that stage
@@ -357,21 +359,30 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
         const bool first = flags & 1, last = (flags >> 1) & 1;
         const uint32_t st = j & 1, ph = (j >> 1) & 1;  // Q/dO stage and dQ buffer
         if (is_a) {
-          // S = Q K^T and dP = dO V^T, interleaved K step by K step
+          // S = Q K^T, then dP = dO V^T
           if (first && !wait_bar_warp(sh, KV_FULL, seg & 1, a.status)) break;
           if (!wait_bar_warp(sh, S_EMPTY, (j & 1) ^ 1, a.status)) break;
-          if (!wait_bar_warp(sh, Q_FULL + st, ph, a.status)) break;
-          if (!wait_bar_warp(sh, DO_FULL + st, ph, a.status)) break;
-          tc_fence_after();
           const uint64_t qk = sdesc_sw128(sb + OFF_QDO, 16, 1024) + st * kStageQ;
           const uint64_t kk0 = sdesc_sw128(sb + OFF_K, 16, 1024);
           const uint64_t dok = sdesc_sw128(sb + OFF_QDO + DO_IN_STAGE, 16, 1024) + st * kStageQ;
           const uint64_t vk = sdesc_sw128(sb + OFF_V, 16, 1024);
+          // S as soon as Q has landed, dP once dO has
+          if (!wait_bar_warp(sh, Q_FULL + st, ph, a.status)) break;
+          tc_fence_after();
           if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint64_t ao = (kk >> 2) * 1024 + (kk & 3) * 2, bo = (kk >> 2) * 512 + (kk & 3) * 2;
               umma_bf16(tmem + COL_S, qk + ao, kk0 + bo, ID_S, kk > 0);
+            }
+          }
+          __syncwarp();
+          if (!wait_bar_warp(sh, DO_FULL + st, ph, a.status)) break;
+          tc_fence_after();
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ao = (kk >> 2) * 1024 + (kk & 3) * 2, bo = (kk >> 2) * 512 + (kk & 3) * 2;
               umma_bf16(tmem + COL_DP, dok + ao, vk + bo, ID_S, kk > 0);
             }
             umma_commit(&sh->bar[S_FULL]);

@@ -12,7 +12,8 @@ phase parity:
 * dK/dV in TMEM per segment.
 
 This model replays each role's order of waits, arrivals, loads and GEMM
-groups under random interleavings.  Each issuer's GEMMs complete in its own
+groups under random interleavings (issuer A: S, then dP; issuer B: dV/dK,
+which releases the Q/dO stage, then dQ).  Each issuer's GEMMs complete in its own
 issue order, and the two issuers complete in any relative order.  Two softmax
 warps stand in for sixteen and two reduce warps for four.  The model asserts
 that every parity wait sees the awaited or just-completed phase.  It asserts
@@ -147,9 +148,10 @@ def _simulate(n_tasks, seed, swap_release=False):
                 yield
             while not B[f"q_full{st}"].ready_parity((j >> 1) & 1, j >> 1):
                 yield
+            qA.append(("S", j))              # S as soon as Q has landed
             while not B[f"do_full{st}"].ready_parity((j >> 1) & 1, j >> 1):
                 yield
-            qA.append(("SdP", j))
+            qA.append(("dP", j))
         yield from get_info("A", n_tasks)
 
     def issuer_b():
@@ -212,11 +214,14 @@ def _simulate(n_tasks, seed, swap_release=False):
 
     def run_a():
         if qA and rng.random() < 0.3:
-            _, j = qA.pop(0)
+            kind, j = qA.pop(0)
             seg, first, last = tasks[j]
-            assert smQ[j & 1] == j and smDO[j & 1] == j, "S/dP before its Q/dO landed"
             assert smKV[0] == seg, "S/dP before its K/V landed"
             assert j == 0 or sdp_read.get(j - 1, 0) == N_SOFT, "S/dP over an S/dP not yet read"
+            if kind == "S":
+                assert smQ[j & 1] == j, "S before its Q landed"
+                return
+            assert smQ[j & 1] == j and smDO[j & 1] == j, "dP before its dO landed"
             tmSdP[0] = j
             doneA.add(j)
             B["s_full"].arrive()
