@@ -10,7 +10,7 @@
 //               a 2-stage ring.
 //   warp 2      MMA issuer A: S = Q K^T as soon as Q has landed, then
 //               dP = dO V^T once dO has.
-//   warp 3      MMA issuer B: dV^T += dO^T P, dK^T += Q^T dS and
+//   warp 3      MMA issuer B: dK^T += Q^T dS, dV^T += dO^T P and
 //               dQ = dS K.  Two issuing threads keep the tensor core fed while
 //               each waits on its own dependencies; their TMEM targets are
 //               disjoint and every cross-phase ordering goes through an
@@ -25,12 +25,15 @@
 //               bulk reduce-add.
 //
 // Issuer A issues S, then dP (each its own accumulator chain, so S can start
-// before the dO tile lands); issuer B interleaves dV^T with dK^T K step by K
-// step, then issues dQ.
+// before the dO tile lands); issuer B issues the dK^T chain, then the dV^T
+// chain, then dQ, and waits for every buffer it needs before it waits for
+// P/dS, so that nothing but the hand-off itself separates P/dS landing from
+// the first MMA.
 //
-// A task's Q/dO stage is held from its TMA load until its dV^T and dK^T MMAs
-// have run (dQ reads only dS and K), so the next task's load into that stage
-// starts before the dQ MMAs.  dQ is double-buffered in TMEM, so the dQ MMAs
+// A task's Q tile is held from its TMA load until its dK^T MMAs have run and
+// its dO tile until its dV^T MMAs have (dQ reads only dS and K), so the load
+// of the task two ahead into the Q half starts one chain before the dO half,
+// and both start before the dQ MMAs.  dQ is double-buffered in TMEM, so the dQ MMAs
 // of task j+1 never wait for the drain of task j.
 //
 // TMEM (512 columns): S at 0, dP at 64, dQ[2] at 128/256 (128 cols each),
@@ -390,14 +393,14 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           }
           __syncwarp();
         } else {
-          // dV^T += dO^T P and dK^T += Q^T dS, interleaved, then dQ = dS K.
-          // P/dS are stored after S/dP completed, so once dV and dK have run
-          // no MMA of the task reads this Q/dO stage any more: it is released
-          // before dQ (which reads dS and K only), and the next load into it
-          // starts a dQ group earlier.
-          if (!wait_bar_warp(sh, PDS_FULL, j & 1, a.status)) break;
+          // dK^T += Q^T dS, then dV^T += dO^T P, then dQ = dS K.  P/dS are
+          // stored after S/dP completed, so once dK has run no MMA of the task
+          // reads its Q tile and once dV has run none reads its dO tile: each
+          // half of the stage is released as soon as its chain is done (a
+          // single warp-issued chain runs as fast as two interleaved ones).
           if (first && !wait_bar_warp(sh, DKV_EMPTY, (seg & 1) ^ 1, a.status)) break;
           if (!wait_bar_warp(sh, DQ_EMPTY + st, ph ^ 1, a.status)) break;
+          if (!wait_bar_warp(sh, PDS_FULL, j & 1, a.status)) break;
           tc_fence_after();
           const uint32_t acc0 = first ? 0u : 1u;
           const uint64_t dom = sdesc_sw128(sb + OFF_QDO + DO_IN_STAGE, 16384, 1024) + st * kStageQ;
@@ -409,11 +412,12 @@ __global__ void __launch_bounds__(ws::kThreads, 1)
           const uint32_t dq = tmem + col_dq(st);
           if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              umma_bf16(tmem + COL_DV, dom + kk * 128, pm + kk * 128, ID_T, kk > 0 ? 1u : acc0);
+            for (int kk = 0; kk < 8; ++kk)
               umma_bf16(tmem + COL_DK, qm + kk * 128, dsm + kk * 128, ID_T, kk > 0 ? 1u : acc0);
-            }
             umma_commit(&sh->bar[Q_EMPTY + st]);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16(tmem + COL_DV, dom + kk * 128, pm + kk * 128, ID_T, kk > 0 ? 1u : acc0);
             umma_commit(&sh->bar[DO_EMPTY + st]);
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) umma_bf16(dq, dsk + k4 * 2, km + k4 * 128, ID_Q, k4 > 0);

@@ -12,8 +12,9 @@ phase parity:
 * dK/dV in TMEM per segment.
 
 This model replays each role's order of waits, arrivals, loads and GEMM
-groups under random interleavings (issuer A: S, then dP; issuer B: dV/dK,
-which releases the Q/dO stage, then dQ).  Each issuer's GEMMs complete in its own
+groups under random interleavings (issuer A: S, then dP; issuer B, once its
+dQ buffer (and at a segment start dK/dV) is free and then P/dS are stored:
+dK, which releases the Q tile, dV, which releases the dO tile, then dQ).  Each issuer's GEMMs complete in its own
 issue order, and the two issuers complete in any relative order.  Two softmax
 warps stand in for sixteen and two reduce warps for four.  The model asserts
 that every parity wait sees the awaited or just-completed phase.  It asserts
@@ -62,7 +63,9 @@ def _segments(rng, n_tasks):
     return out
 
 
-def _simulate(n_tasks, seed, swap_release=False):
+def _simulate(n_tasks, seed, early_do_release=False):
+    # early_do_release: a mutation that releases the dO tile with the Q tile
+    # after dK, before the dV chain that reads it has run
     rng = random.Random(seed)
     tasks = _segments(rng, n_tasks)
     B = {}
@@ -88,7 +91,7 @@ def _simulate(n_tasks, seed, swap_release=False):
     tmDQ = [None, None]
     tmDKV = [None]                    # segment whose dK/dV accumulate in TMEM
     doneA, doneB = set(), set()       # completed GEMM groups (S/dP; dV/dK and dQ)
-    releasedB = set()                 # tasks whose dV/dK completed (Q/dO stage released)
+    releasedQ, releasedDO = set(), set()  # tasks whose dK / dV completed (Q / dO tile released)
     sdp_read, pds_written = {}, {}    # task -> softmax warps done reading S/dP / writing P/dS
     dq_read, dkv_read = {}, {}        # task / segment -> reduce warps done
     qA, qB, tma = [], [], []
@@ -159,14 +162,15 @@ def _simulate(n_tasks, seed, swap_release=False):
             yield from get_info("B", j)
             seg, first, last = tasks[j]
             st = j & 1
-            while not B["pds_full"].ready_parity(j & 1, j):
-                yield
             if first:
                 while not B["dkv_empty"].ready_parity((seg & 1) ^ 1, seg - 1):
                     yield
             while not B[f"dq_empty{st}"].ready_parity(((j >> 1) & 1) ^ 1, (j >> 1) - 1):
                 yield
-            qB.append(("dVdK", j))
+            while not B["pds_full"].ready_parity(j & 1, j):
+                yield
+            qB.append(("dK", j))
+            qB.append(("dV", j))
             qB.append(("dQ", j))
         yield from get_info("B", n_tasks)
 
@@ -233,17 +237,23 @@ def _simulate(n_tasks, seed, swap_release=False):
             kind, j = qB.pop(0)
             seg, first, last = tasks[j]
             assert smPdS[0] == j and pds_written.get(j, 0) == N_SOFT, "dV/dK/dQ before P/dS were stored"
-            if kind == "dVdK":
-                # dV^T and dK^T read the Q/dO stage, P and dS; the stage is
-                # released when they complete
-                assert smQ[j & 1] == j and smDO[j & 1] == j, "dV/dK after the Q/dO stage was reloaded"
+            if kind == "dK":
+                # dK^T reads the Q tile and dS; the Q tile is released when it completes
+                assert smQ[j & 1] == j, "dK after the Q tile was reloaded"
                 if first:
                     assert seg == 0 or dkv_read.get(seg - 1, 0) == N_RED, "dK/dV overwritten before drained"
                     tmDKV[0] = seg
-                releasedB.add(j)
-                for n in ([f"do_empty{j & 1}", f"q_empty{j & 1}"] if swap_release else
-                          [f"q_empty{j & 1}", f"do_empty{j & 1}"]):
-                    B[n].arrive()
+                releasedQ.add(j)
+                B[f"q_empty{j & 1}"].arrive()
+                if early_do_release:
+                    B[f"do_empty{j & 1}"].arrive()
+                return
+            if kind == "dV":
+                # dV^T reads the dO tile and P; the dO tile is released when it completes
+                assert smDO[j & 1] == j, "dV after the dO tile was reloaded"
+                releasedDO.add(j)
+                if not early_do_release:
+                    B[f"do_empty{j & 1}"].arrive()
                 return
             # dQ reads dS and K
             assert smKV[0] == seg, "dQ after K was reloaded"
@@ -265,11 +275,11 @@ def _simulate(n_tasks, seed, swap_release=False):
                 smKV[0] = x
                 B["kv"].arrive()
             elif kind == "q":
-                assert x < 2 or ((x - 2) in doneA and (x - 2) in releasedB), "Q stage reloaded too early"
+                assert x < 2 or ((x - 2) in doneA and (x - 2) in releasedQ), "Q stage reloaded too early"
                 smQ[x & 1] = x
                 B[f"q_full{x & 1}"].arrive()
             else:
-                assert x < 2 or ((x - 2) in doneA and (x - 2) in releasedB), "dO stage reloaded too early"
+                assert x < 2 or ((x - 2) in doneA and (x - 2) in releasedDO), "dO stage reloaded too early"
                 smDO[x & 1] = x
                 B[f"do_full{x & 1}"].arrive()
 
@@ -299,3 +309,83 @@ def test_backward_protocol_holds_under_random_schedules():
     rng = random.Random(0)
     for seed in range(400):
         _simulate(rng.randint(1, 24), seed)
+
+
+def test_protocol_model_catches_an_early_do_release():
+    """Releasing the dO tile with the Q tile, after dK, lets the next load
+    overwrite dO while the dV chain may still read it, and the model sees it."""
+    rng = random.Random(0)
+    caught = 0
+    for seed in range(200):
+        try:
+            _simulate(rng.randint(3, 24), seed, early_do_release=True)
+        except AssertionError as e:
+            assert "reloaded" in str(e)
+            caught += 1
+    assert caught > 0
+
+
+def _reduce_staging(flags, seed, dq_commits=True, dq_wait_keep=1):
+    """One reduce warp's two staging slots over a task sequence (flags[j]: task
+    j ends a bucket segment).  Per task the warp writes both 64-dim dQ halves,
+    then a segment end adds four dK/dV chunks; chunk n uses slot n & 1.  A
+    chunk read by a bulk reduce-add is committed as its own group (dK/dV
+    always; dQ when dq_commits, as the kernel does; a path that read its dQ
+    slot back itself would commit none).  Before writing a slot the warp runs
+    `cp.async.bulk.wait_group.read N` (N = dq_wait_keep for dQ, 1 for dK/dV):
+    afterwards only the N most recently committed groups may still be reading.
+    Pending groups finish reading in any order, at random.  Returns the first
+    write into a slot that a pending group still reads, or None."""
+    rng = random.Random(seed)
+    pending = {}  # group index -> slot it reads
+    committed = 0
+    chunk = 0
+
+    def wait_read(keep):
+        for g in [g for g in pending if g < committed - keep]:
+            del pending[g]
+
+    def progress():
+        for g in list(pending):
+            if rng.random() < 0.3:
+                del pending[g]
+
+    def use(kind, j, i, keep, commit):
+        nonlocal committed, chunk
+        progress()
+        wait_read(keep)
+        if (chunk & 1) in pending.values():
+            return (kind, j, i)
+        if commit:
+            pending[committed] = chunk & 1
+            committed += 1
+        chunk += 1
+        return None
+
+    for j, last in enumerate(flags):
+        for hf in range(2):
+            bad = use("dq", j, hf, dq_wait_keep, dq_commits)
+            if bad:
+                return bad
+        if last:
+            for q in range(4):
+                bad = use("dkv", j, q, 1, True)
+                if bad:
+                    return bad
+    return None
+
+
+def test_reduce_staging_slots_are_never_overwritten_while_read():
+    """Every staged chunk is one bulk group and each write waits until at most
+    the newest group is still reading, so the slot written (the other one's
+    twin) is never still read.  The same wait after a chunk that commits no
+    group is not enough (the newest group may be reading the slot about to be
+    written), and the model catches that; waiting for every group is."""
+    rng = random.Random(1)
+    caught = 0
+    for seed in range(2000):
+        flags = [rng.random() < 0.3 for _ in range(rng.randint(1, 12))]
+        assert _reduce_staging(flags, seed) is None
+        assert _reduce_staging(flags, seed, dq_commits=False, dq_wait_keep=0) is None
+        caught += _reduce_staging(flags, seed, dq_commits=False, dq_wait_keep=1) is not None
+    assert caught > 0
