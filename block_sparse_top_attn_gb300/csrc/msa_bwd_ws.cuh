@@ -20,9 +20,10 @@
 //               columns 16*((w-4)/4)..; four per SM sub-partition, so the
 //               latency of one warp's exp/convert chain hides behind others'.
 //   warps 20-23 reduce: dQ per task and dK/dV per segment, TMEM -> swizzled
-//               fp32 staging (two 4 KB slots per warp, so a slot is refilled
-//               while the reduce-add of the other is still reading) -> TMA
-//               bulk reduce-add.
+//               staging (bf16 dQ, or fp32 with the fp32 dQ option; fp32 dK/dV;
+//               two 4 KB slots per warp, so a slot is refilled while the
+//               reduce-add of the other is still reading) -> TMA bulk
+//               reduce-add.
 //
 // Issuer A issues S, then dP (each its own accumulator chain, so S can start
 // before the dO tile lands); issuer B issues the dK^T chain, then the dV^T
@@ -33,8 +34,8 @@
 // A task's Q tile is held from its TMA load until its dK^T MMAs have run and
 // its dO tile until its dV^T MMAs have (dQ reads only dS and K), so the load
 // of the task two ahead into the Q half starts one chain before the dO half,
-// and both start before the dQ MMAs.  dQ is double-buffered in TMEM, so the dQ MMAs
-// of task j+1 never wait for the drain of task j.
+// and both start before the dQ MMAs.  dQ is double-buffered in TMEM, so the
+// dQ MMAs of task j+1 never wait for the drain of task j.
 //
 // TMEM (512 columns): S at 0, dP at 64, dQ[2] at 128/256 (128 cols each),
 // dK^T at 384, dV^T at 448 (64 cols each; lane = head-dim index).

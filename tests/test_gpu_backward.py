@@ -201,10 +201,12 @@ def _dq_repeat_bound(pb, units, G):
 
 @pytest.mark.parametrize("name,tile", [("tiny", 0), ("single8k", 0), ("single8k", 16), ("zipf64k", 512)])
 def test_backward_is_repeatable_within_tolerance(B, name, tile):
-    """Three runs on the same inputs: dK and dV (fp32 accumulation, then one
-    rounding) agree to two bf16 ulps; dQ, reduced in bf16 in whatever order the
-    L2 applies the adds, agrees within the bound n ulp(M) that the order alone
-    allows (see _dq_repeat_bound) on sampled rows, and within a relative
+    """Three runs on the same inputs: dK and dV (fp32 partial sums per bucket
+    segment, added across segments by fp32 reduce-adds in the L2's order, then
+    one rounding) agree to two bf16 ulps of the element or of 1/256 of its
+    row's largest magnitude, whichever is larger; dQ, reduced in bf16 in
+    whatever order the L2 applies the adds, agrees within the bound n ulp(M)
+    that the order alone allows (see _dq_repeat_bound) on sampled rows, and within a relative
     Frobenius 5e-3 overall.  A pipeline race (an operand used before it lands,
     a buffer overwritten while read) shows up here even when it happens to stay
     inside the oracle tolerance.  zipf64k is the skewed workload: its hot key
@@ -244,5 +246,12 @@ def test_backward_is_repeatable_within_tolerance(B, name, tile):
                 for rows, hs, _, _, bound in bounds:
                     assert np.all(np.abs(x[rows][:, hs] - y[rows][:, hs]) <= bound), (name_, rows[0])
             else:
-                ulp = O.bf16_ulp(np.maximum(np.abs(x), 1e-3))
+                # Where a row's segment partials nearly cancel, the order of the
+                # fp32 adds alone moves a small element by more than an ulp of
+                # itself (measured on zipf64k: up to two, now and then more), but
+                # by only a few fp32 ulps of the partials, far below an ulp of
+                # 1/256 of the row's scale; a lost or doubled contribution (a
+                # race) moves it by about the row's scale and still fails here.
+                scale = np.maximum(np.abs(x), np.max(np.abs(x), axis=-1, keepdims=True) / 256.0)
+                ulp = O.bf16_ulp(np.maximum(scale, 1e-3))
                 assert np.all(np.abs(x - y) <= 2 * ulp), name_
