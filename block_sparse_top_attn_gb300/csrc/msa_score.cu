@@ -16,7 +16,7 @@
 //   to the lower block, then -1.
 //
 // Kernels: pool_kernel (one warp per chunk or block and index head; HBM-bound)
-// and topk_kernel (a CTA scores 32 chunks against 64-block tiles with a 4 x 2
+// and topk_kernel (a CTA scores 64 chunks against 64-block tiles with an 8 x 2
 // register tile per thread, four dims per step, then each warp merges its
 // rows' candidates into per-row top-(K-1) lists held one entry per lane).
 #include <cuda_runtime.h>
@@ -30,9 +30,10 @@ namespace msa {
 namespace score {
 
 constexpr int kDim = 128;        // index dim
-constexpr int kRows = 32;        // chunks per CTA
+constexpr int kRows = 64;        // chunks per CTA
 constexpr int kCols = 64;        // blocks per tile
 constexpr int kThreads = 256;
+constexpr int kWarpRows = kRows / (kThreads / 32);  // rows (chunks) of one warp's register tile
 // dynamic shared memory: pooled queries [kRows][kDim] and a transposed key
 // tile [kDim][kCols] in fp32, then the rows' candidate ranges
 constexpr uint32_t SMEM = (kRows * kDim + kDim * kCols) * 4 + 2 * kRows * 4;
@@ -137,12 +138,12 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
       blo = min(blo, s_lo[r]);
       bhi = max(bhi, s_lo[r] + s_n[r]);
     }
-  // per-row top-(K-1) lists: lane i holds entry i of each of the warp's 4 rows
+  // per-row top-(K-1) lists: lane i holds entry i of each of the warp's rows
   const int keep = a.K - 1;
-  float ls[4];
-  int lb[4];
+  float ls[kWarpRows];
+  int lb[kWarpRows];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) { ls[i] = -CUDART_INF_F; lb[i] = INT32_MAX; }
+  for (int i = 0; i < kWarpRows; ++i) { ls[i] = -CUDART_INF_F; lb[i] = INT32_MAX; }
   for (int b0 = blo; b0 < bhi; b0 += kCols) {
     __syncthreads();  // the previous tile is no longer read
     {
@@ -162,21 +163,21 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
       }
     }
     __syncthreads();
-    // 4 rows (4 warp .. 4 warp + 3) x 2 blocks (b0 + 2 lane, + 1), summed over
-    // the dims in ascending order
-    // (four dims per step: a row's four query values in one 16-byte load, so
-    // eight shared-memory loads feed 32 FMAs)
-    float s[4][2];
+    // kWarpRows rows (from kWarpRows * warp) x 2 blocks (b0 + 2 lane, + 1),
+    // summed over the dims in ascending order (four dims per step: a row's
+    // four query values in one 16-byte load that every lane shares, so twelve
+    // shared-memory loads feed 64 FMAs)
+    float s[kWarpRows][2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s[i][0] = s[i][1] = 0.f;
+    for (int i = 0; i < kWarpRows; ++i) s[i][0] = s[i][1] = 0.f;
 #pragma unroll 2
     for (int d = 0; d < kDim; d += 4) {
       float2 kv[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) kv[e] = *reinterpret_cast<const float2*>(&sk[d + e][2 * lane]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 q4 = *reinterpret_cast<const float4*>(&sq[4 * warp + i][d]);
+      for (int i = 0; i < kWarpRows; ++i) {
+        const float4 q4 = *reinterpret_cast<const float4*>(&sq[kWarpRows * warp + i][d]);
         const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -187,8 +188,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     }
     // merge each row's candidates of this tile into its list
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = 4 * warp + i;
+    for (int i = 0; i < kWarpRows; ++i) {
+      const int r = kWarpRows * warp + i;
       const int lo = s_lo[r], n = s_n[r];
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj) {
@@ -222,8 +223,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
   }
   // write the rows: diagonal, the kept blocks (document-local), -1 pads
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = 4 * warp + i, g = g0 + r;
+  for (int i = 0; i < kWarpRows; ++i) {
+    const int r = kWarpRows * warp + i, g = g0 + r;
     if (g >= a.NC) continue;
     const int lo = s_lo[r];
     int32_t* row = a.sel + ((int64_t)hi * a.NC + g) * a.K;
